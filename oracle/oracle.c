@@ -1,0 +1,331 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle of the paged-attention decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library. The CUDA path never calls it,
+ * shares no code with it and must not fall back to it.
+ *
+ * What it computes, step by step, and where each step is defined:
+ *
+ *  cache write   Each new token's K and V vectors go to their slot: block
+ *                slot / block_size, offset slot % block_size. Raw 16-bit words
+ *                are copied; nothing is converted. (yangyu.win blog #54,
+ *                section 5 question 2: a sequence that grows past a block
+ *                boundary takes one new block from the free pool; itimpress.au
+ *                "PagedAttention, ...", section 1: K and V of every previous
+ *                token are kept so they are not recomputed.)
+ *  gather        Logical token t of a sequence lives in physical block
+ *                block_table[t / block_size] at offset t % block_size.
+ *                (yangyu.win blog #54, section 2.2 figure: tokens 0-15 -> page 7,
+ *                16-31 -> page 2, 32-47 -> page 19; learn.tanhdev.com part 8,
+ *                block-table diagram: virtual 0 -> #42, 1 -> #108, 2 -> #19.)
+ *  attention     A_i = softmax(q_i K^T / sqrt(d_k)), o_i = sum over blocks j and
+ *                slots t of a_{i,j,t} v_{(j,t)}. (learn.tanhdev.com part 8,
+ *                section "Thuc thi kernel toan hoc trong CUDA", equations for A_i,
+ *                A_{i,j} and o_i.) GQA: query head h reads KV head h / (Hq / Hkv)
+ *                (contiguous groups; the pages name GQA, not the mapping).
+ *                With q_len > 1 (verifying draft tokens in one pass:
+ *                itimpress.au section 1, yangyu.win section 2.4) query row qi sits
+ *                at position L - q_len + qi and sees tokens 0 .. L - q_len + qi.
+ *  partitions    The context is cut into fixed partitions; each yields its own
+ *                (max, sum of exponentials, unnormalised weighted V), and a
+ *                reduction combines them (maths.nthquan ch. 17 "Scaling and
+ *                deployment", section "Sequence parallelism": local attention
+ *                per cached segment, then a reduction). The combination is the
+ *                log-sum-exp merge written out from the softmax definition.
+ *
+ * All arithmetic is fp64. fp16/bf16 inputs are decoded exactly from their bit
+ * patterns. The softmax subtracts the maximum score first (the same value,
+ * written to avoid overflow). Nothing is blocked, fused or reordered beyond
+ * these definitions.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define OR_OK 0
+#define OR_ERR_ARG 1
+#define OR_ERR_BOUNDS 2
+#define OR_ERR_OOM 3
+
+#define OR_FP16 0
+#define OR_BF16 1
+
+/* ---------------------------------------------------------------- decoding */
+
+/* IEEE binary16: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+double oracle_f16_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);    /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double dec(uint16_t w, int dtype) {
+    return dtype == OR_BF16 ? oracle_bf16_to_double(w) : oracle_f16_to_double(w);
+}
+
+/* ------------------------------------------------------------- cache write */
+
+/* k, v: [num_tokens, Hkv, d]; pools: [num_blocks, Hkv, bs, d]. slot < 0 is skipped. */
+int oracle_cache_write(uint16_t *k_pool, uint16_t *v_pool, const uint16_t *k, const uint16_t *v,
+                       const int64_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                       int bs, int Hkv, int d) {
+    if (!k_pool || !v_pool || !k || !v || !slot_mapping || bs <= 0 || Hkv <= 0 || d <= 0)
+        return OR_ERR_ARG;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        int64_t blk = s / bs, off = s % bs;
+        if (blk >= num_blocks) return OR_ERR_BOUNDS;
+        for (int h = 0; h < Hkv; ++h) {
+            int64_t src = (i * Hkv + h) * (int64_t)d;
+            int64_t dst = ((blk * Hkv + h) * bs + off) * (int64_t)d;
+            memcpy(k_pool + dst, k + src, (size_t)d * sizeof(uint16_t));
+            memcpy(v_pool + dst, v + src, (size_t)d * sizeof(uint16_t));
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ gather */
+
+/* Contiguous [L, Hkv, d] copy of one sequence's K (or V) through its block-table row. */
+int oracle_gather(const uint16_t *pool, const int32_t *table_row, int64_t L, int64_t num_blocks,
+                  int bs, int Hkv, int d, uint16_t *out) {
+    if (!pool || !table_row || !out || L < 0 || bs <= 0) return OR_ERR_ARG;
+    for (int64_t t = 0; t < L; ++t) {
+        int64_t phys = table_row[t / bs];
+        int64_t off = t % bs;
+        if (phys < 0 || phys >= num_blocks) return OR_ERR_BOUNDS;
+        for (int h = 0; h < Hkv; ++h)
+            memcpy(out + (t * Hkv + h) * (int64_t)d, pool + ((phys * Hkv + h) * bs + off) * (int64_t)d,
+                   (size_t)d * sizeof(uint16_t));
+    }
+    return OR_OK;
+}
+
+/* --------------------------------------------------------------- attention */
+
+/*
+ * One sequence on contiguous K/V.
+ *   q   [q_len, Hq, d]     kc, vc  [L, Hkv, d]     out  [q_len, Hq, d] (double)
+ *   weights (optional) [q_len, Hq, L]: the softmax weights, 0 for masked tokens.
+ */
+int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int64_t L, int q_len,
+                     int Hq, int Hkv, int d, int dtype, float scale, double *out, double *weights) {
+    if (!q || !kc || !vc || !out || q_len < 1 || L < q_len || Hkv <= 0 || Hq % Hkv != 0 || d <= 0)
+        return OR_ERR_ARG;
+    int G = Hq / Hkv;
+    double *s = (double *)malloc((size_t)L * sizeof(double));
+    double *qd = (double *)malloc((size_t)d * sizeof(double));
+    if (!s || !qd) { free(s); free(qd); return OR_ERR_OOM; }
+    for (int qi = 0; qi < q_len; ++qi) {
+        int64_t last = L - q_len + qi;                     /* inclusive causal limit */
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / G;
+            for (int k = 0; k < d; ++k) qd[k] = dec(q[((int64_t)qi * Hq + h) * d + k], dtype);
+            double mx = -INFINITY;
+            for (int64_t t = 0; t <= last; ++t) {
+                double dot = 0.0;
+                const uint16_t *kr = kc + (t * Hkv + g) * (int64_t)d;
+                for (int k = 0; k < d; ++k) dot += qd[k] * dec(kr[k], dtype);
+                s[t] = (double)scale * dot;
+                if (s[t] > mx) mx = s[t];
+            }
+            double l = 0.0;
+            for (int64_t t = 0; t <= last; ++t) { s[t] = exp(s[t] - mx); l += s[t]; }
+            double *o = out + ((int64_t)qi * Hq + h) * d;
+            for (int k = 0; k < d; ++k) o[k] = 0.0;
+            for (int64_t t = 0; t <= last; ++t) {
+                double p = s[t] / l;
+                const uint16_t *vr = vc + (t * Hkv + g) * (int64_t)d;
+                for (int k = 0; k < d; ++k) o[k] += p * dec(vr[k], dtype);
+            }
+            if (weights) {
+                double *w = weights + ((int64_t)qi * Hq + h) * L;
+                for (int64_t t = 0; t < L; ++t) w[t] = t <= last ? s[t] / l : 0.0;
+            }
+        }
+    }
+    free(s);
+    free(qd);
+    return OR_OK;
+}
+
+/* --------------------------------------------------------- paged attention */
+
+typedef struct {
+    const uint16_t *q, *k_pool, *v_pool;
+    const int32_t *tables;
+    const int32_t *lens;
+    const int32_t *seqs;         /* which sequences to compute (rows of q / out follow this list) */
+    int64_t stride, num_blocks;
+    int nseq, q_len, Hq, Hkv, d, bs, dtype;
+    float scale;
+    double *out;
+    int next;                    /* work counter */
+    int err;
+    pthread_mutex_t mu;
+} paged_job;
+
+static void *paged_worker(void *arg) {
+    paged_job *J = (paged_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int i = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (i >= J->nseq) break;
+        int b = J->seqs ? J->seqs[i] : i;
+        int64_t L = J->lens[b];
+        size_t n = (size_t)L * J->Hkv * J->d;
+        uint16_t *kc = (uint16_t *)malloc(n * sizeof(uint16_t));
+        uint16_t *vc = (uint16_t *)malloc(n * sizeof(uint16_t));
+        int rc = (!kc || !vc) ? OR_ERR_OOM : OR_OK;
+        const int32_t *row = J->tables + (int64_t)b * J->stride;
+        if (rc == OR_OK && (L + J->bs - 1) / J->bs > J->stride) rc = OR_ERR_BOUNDS;
+        if (rc == OR_OK) rc = oracle_gather(J->k_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, kc);
+        if (rc == OR_OK) rc = oracle_gather(J->v_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, vc);
+        if (rc == OR_OK)
+            rc = oracle_attention(J->q + (int64_t)i * J->q_len * J->Hq * J->d, kc, vc, L, J->q_len, J->Hq,
+                                  J->Hkv, J->d, J->dtype, J->scale,
+                                  J->out + (int64_t)i * J->q_len * J->Hq * J->d, NULL);
+        free(kc);
+        free(vc);
+        if (rc != OR_OK) {
+            pthread_mutex_lock(&J->mu);
+            if (!J->err) J->err = rc;
+            pthread_mutex_unlock(&J->mu);
+        }
+    }
+    return NULL;
+}
+
+int oracle_num_cpus(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/*
+ * Paged decode for the sequences listed in seqs (or all num_seqs when seqs is NULL):
+ * gather each sequence through its block-table row, then attention.
+ *   q, out: one [q_len, Hq, d] row per listed sequence, in list order.
+ *   Returns the number of threads used through *threads_used (may be NULL).
+ */
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *block_tables, int64_t stride, const int32_t *context_lens,
+                           const int32_t *seqs, int nseq, int64_t num_blocks, int bs, int q_len, int Hq,
+                           int Hkv, int d, int dtype, float scale, double *out, int num_threads,
+                           int *threads_used) {
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || nseq < 0) return OR_ERR_ARG;
+    paged_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k_pool = k_pool; J.v_pool = v_pool; J.tables = block_tables; J.lens = context_lens;
+    J.seqs = seqs; J.stride = stride; J.num_blocks = num_blocks; J.nseq = nseq; J.q_len = q_len;
+    J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.bs = bs; J.dtype = dtype; J.scale = scale; J.out = out;
+    pthread_mutex_init(&J.mu, NULL);
+    int nt = num_threads > 0 ? num_threads : oracle_num_cpus();
+    if (nt > nseq) nt = nseq > 0 ? nseq : 1;
+    pthread_t *th = (pthread_t *)malloc((size_t)nt * sizeof(pthread_t));
+    if (!th) return OR_ERR_OOM;
+    for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, paged_worker, &J);
+    for (int i = 0; i < nt; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.mu);
+    if (threads_used) *threads_used = nt;
+    return J.err;
+}
+
+/* ------------------------------------------------ partitions and the merge */
+
+/*
+ * One sequence on contiguous K/V, context cut into partitions of P tokens.
+ * For partition p (tokens [pP, min((p+1)P, L)) that row qi may see):
+ *   m[p]  = max score            (-inf when the row sees none of them)
+ *   l[p]  = sum exp(s_t - m[p])  (0 when empty)
+ *   o[p]  = sum exp(s_t - m[p]) v_t   (unnormalised; 0 when empty)
+ * Layouts: m, l [q_len, Hq, np]; o [q_len, Hq, np, d], np = ceil(L / P).
+ */
+int oracle_attention_partitions(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int64_t L,
+                                int q_len, int Hq, int Hkv, int d, int dtype, float scale, int64_t P,
+                                double *m, double *l, double *o) {
+    if (!q || !kc || !vc || !m || !l || !o || P <= 0 || q_len < 1 || L < q_len || Hq % Hkv != 0)
+        return OR_ERR_ARG;
+    int G = Hq / Hkv;
+    int64_t np_ = (L + P - 1) / P;
+    double *s = (double *)malloc((size_t)P * sizeof(double));
+    if (!s) return OR_ERR_OOM;
+    for (int qi = 0; qi < q_len; ++qi) {
+        int64_t last = L - q_len + qi;
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / G;
+            const uint16_t *qr = q + ((int64_t)qi * Hq + h) * d;
+            for (int64_t p = 0; p < np_; ++p) {
+                int64_t row = ((int64_t)qi * Hq + h) * np_ + p;
+                int64_t t0 = p * P, t1 = (p + 1) * P < L ? (p + 1) * P : L;
+                if (t1 > last + 1) t1 = last + 1;
+                double mx = -INFINITY, sum = 0.0;
+                double *op = o + row * d;
+                for (int k = 0; k < d; ++k) op[k] = 0.0;
+                for (int64_t t = t0; t < t1; ++t) {
+                    double dot = 0.0;
+                    const uint16_t *kr = kc + (t * Hkv + g) * (int64_t)d;
+                    for (int k = 0; k < d; ++k) dot += dec(qr[k], dtype) * dec(kr[k], dtype);
+                    s[t - t0] = (double)scale * dot;
+                    if (s[t - t0] > mx) mx = s[t - t0];
+                }
+                for (int64_t t = t0; t < t1; ++t) {
+                    double e = exp(s[t - t0] - mx);
+                    sum += e;
+                    const uint16_t *vr = vc + (t * Hkv + g) * (int64_t)d;
+                    for (int k = 0; k < d; ++k) op[k] += e * dec(vr[k], dtype);
+                }
+                m[row] = mx;
+                l[row] = sum;
+            }
+        }
+    }
+    free(s);
+    return OR_OK;
+}
+
+/*
+ * Log-sum-exp merge of np partitions of one output row:
+ *   M = max over non-empty partitions of m[p]
+ *   out = sum_p exp(m[p] - M) o[p] / sum_p exp(m[p] - M) l[p]
+ * m, l: [np]; o: [np, d]; out: [d].
+ */
+int oracle_lse_merge(int64_t np_, const double *m, const double *l, const double *o, int d, double *out) {
+    if (!m || !l || !o || !out || np_ < 1) return OR_ERR_ARG;
+    double M = -INFINITY;
+    for (int64_t p = 0; p < np_; ++p)
+        if (l[p] > 0.0 && m[p] > M) M = m[p];
+    double den = 0.0;
+    for (int k = 0; k < d; ++k) out[k] = 0.0;
+    for (int64_t p = 0; p < np_; ++p) {
+        if (!(l[p] > 0.0)) continue;
+        double w = exp(m[p] - M);
+        den += w * l[p];
+        for (int k = 0; k < d; ++k) out[k] += w * o[p * d + k];
+    }
+    for (int k = 0; k < d; ++k) out[k] /= den;
+    return OR_OK;
+}

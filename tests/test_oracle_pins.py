@@ -1,0 +1,78 @@
+"""The oracle against its pins, and the pins against planted mistakes.
+
+Every pin runs against the real oracle and must pass. Then each entry of
+MUTANTS plants one plausible mistake in a copy of oracle.c (a dropped term, a
+wrong index or sign, a transposed operand), builds it on the CPU, and the pin
+suite must fail on it.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+MUTANTS = {
+    "drop_scale": ("s[t] = (double)scale * dot;", "s[t] = dot;"),
+    "gqa_modulo": ("            int g = h / G;\n            for (int k = 0; k < d; ++k) qd[k]",
+                   "            int g = h % Hkv;\n            for (int k = 0; k < d; ++k) qd[k]"),
+    "no_causal_limit": ("        int64_t last = L - q_len + qi;                     /* inclusive causal limit */",
+                        "        int64_t last = L - 1;"),
+    "causal_off_by_one": ("        int64_t last = L - q_len + qi;                     /* inclusive causal limit */",
+                          "        int64_t last = L - q_len + qi - (qi > 0);"),
+    "gather_wrong_block": ("int64_t phys = table_row[t / bs];", "int64_t phys = table_row[t % bs];"),
+    "gather_wrong_offset": ("int64_t off = t % bs;\n", "int64_t off = t / bs % bs;\n"),
+    "no_normalise": ("double p = s[t] / l;", "double p = s[t];"),
+    "dot_reads_v": ("const uint16_t *kr = kc + (t * Hkv + g) * (int64_t)d;\n                for (int k = 0; k < d; ++k) dot += qd[k]",
+                    "const uint16_t *kr = vc + (t * Hkv + g) * (int64_t)d;\n                for (int k = 0; k < d; ++k) dot += qd[k]"),
+    "no_max_shift_bug": ("{ s[t] = exp(s[t] - mx); l += s[t]; }", "{ s[t] = exp(s[t] - mx); l += 1.0; }"),
+    "cache_write_offset": ("int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = 0;"),
+    "cache_write_head_swap": ("int64_t dst = ((blk * Hkv + h) * bs + off) * (int64_t)d;",
+                              "int64_t dst = ((blk * Hkv + (Hkv - 1 - h)) * bs + off) * (int64_t)d;"),
+    "cache_write_no_skip": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
+    "fp16_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "fp16_subnormal": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "bf16_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    "merge_unweighted_den": ("den += w * l[p];", "den += l[p];"),
+    "merge_weight_sign": ("double w = exp(m[p] - M);", "double w = exp(M - m[p]);"),
+    "partition_no_shift": ("double e = exp(s[t - t0] - mx);", "double e = exp(s[t - t0]);"),
+    "partition_tail": ("if (t1 > last + 1) t1 = last + 1;", "if (t1 > last + 2) t1 = last + 2;"),
+    "weights_unmasked": ("w[t] = t <= last ? s[t] / l : 0.0;", "w[t] = t <= last ? s[t] / l : 1e-300;"),
+}
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    oracle.use(None)
+    pin()
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    d = tempfile.mkdtemp(prefix="oracle_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, mutant_dir):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    path = os.path.join(mutant_dir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = oracle.build(force=True, src=path, out=os.path.join(mutant_dir, name + ".so"))
+    oracle.use(so)
+    failed = []
+    try:
+        for pin in pins.ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, RuntimeError):
+                failed.append(pin.__name__)
+    finally:
+        oracle.use(None)
+    assert failed, f"no pin caught mutant {name}"

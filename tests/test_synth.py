@@ -1,0 +1,69 @@
+"""The seeded input generator: its published definitions and the workload recipes."""
+import numpy as np
+
+import synth
+
+
+def test_splitmix64_reference_values():
+    # SplitMix64 with state 0: the first outputs of the published generator (state += gamma; mix).
+    outs, state = [], 0
+    for _ in range(3):
+        outs.append(synth._mix_py(state))
+        state = (state + synth.GAMMA) & synth.MASK64
+    assert outs == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    # the vectorised hash is the same function
+    base = synth.stream_base(7, 9)
+    h = synth.hash64(7, 9, np.arange(4, dtype=np.uint64))
+    assert [int(x) for x in h] == [synth._mix_py((base + i) & synth.MASK64) for i in range(4)]
+
+
+def test_scale_constant():
+    assert float(synth.C_F32) == float(np.float32(np.sqrt(3.0) / 131072.0))
+
+
+def test_values_moments_and_determinism():
+    x = synth.unit_f32(5, 11, np.arange(1 << 20, dtype=np.uint64))
+    assert abs(float(x.mean())) < 5e-3 and abs(float(x.std()) - 1.0) < 5e-3
+    assert np.abs(x).max() <= np.float32(3.4641)
+    a = synth.values16(5, 11, np.arange(1000, dtype=np.uint64), synth.BF16)
+    b = synth.values16(5, 11, np.arange(1000, dtype=np.uint64), synth.BF16)
+    assert np.array_equal(a, b)
+
+
+def test_bf16_rounding_ties_to_even():
+    x = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20], np.float32)
+    w = synth.f32_to_bits16(x, synth.BF16)
+    assert [hex(int(v)) for v in w] == ["0x3f80", "0x3f82", "0xbf80", "0x3f81"]
+
+
+def test_permutation_is_permutation():
+    p = synth.permutation(1, 2, 1000)
+    assert np.array_equal(np.sort(p), np.arange(1000))
+
+
+def test_workload_tables_valid():
+    for k in (1, 2, 4, 5):
+        wl = synth.workload(k, batch=8 if k in (2, 4) else None)
+        used = []
+        for b in range(wl.B):
+            nb = -(-int(wl.context_lens[b]) // wl.bs)
+            row = wl.block_tables[b]
+            assert (row[:nb] >= 0).all() and (row[:nb] < wl.num_blocks).all() and (row[nb:] == -1).all()
+            used.append(row[wl.prefix_tokens // wl.bs:nb])
+        own = np.concatenate(used)
+        assert len(np.unique(own)) == len(own)          # private blocks are never shared
+        if wl.prefix_tokens:
+            assert (wl.block_tables[:, :wl.prefix_tokens // wl.bs] == wl.block_tables[0, :wl.prefix_tokens // wl.bs]).all()
+
+
+def test_workload_shapes():
+    w1 = synth.workload(1)
+    assert list(w1.context_lens) == [17, 64, 100, 200] and w1.num_blocks == 64 and w1.scale == 0.125
+    w2 = synth.workload(2)
+    assert w2.context_lens.min() >= 512 and w2.context_lens.max() <= 4096
+    assert w2.num_blocks == int(np.ceil(1.1 * sum(-(-int(L) // 16) for L in w2.context_lens)))
+    w4 = synth.workload(4)
+    suf = w4.context_lens - 1024
+    assert suf.min() >= 64 and suf.max() <= 512 and w4.q_len == 5
+    w5 = synth.workload(5)
+    assert w5.bs == 32 and w5.num_blocks == 16384
