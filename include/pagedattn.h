@@ -1,0 +1,158 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged-attention decode library.
+ *
+ * The KV cache is one pool of fixed-size physical blocks (16 or 32 tokens);
+ * each sequence's block table maps its logical token blocks to physical block
+ * ids, and the attention kernel looks the table up itself (itimpress.au
+ * "PagedAttention, speculative decoding, MoE and Blackwell", section 1;
+ * yangyu.win blog #54 section 2.2; learn.tanhdev.com "Part 8: Inference
+ * optimization with vLLM", section on executing the kernel math in CUDA).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must point to memory of the pool's
+ *    device, 16-byte aligned, owned by the caller (the library never frees
+ *    them). The library owns only what pa_pool_create allocated.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Work is enqueued asynchronously; no call synchronises except
+ *    pa_pool_check.
+ *  - Argument errors are detected on the host and returned before anything is
+ *    launched. Data errors that only the device can see (a block id outside the
+ *    pool, a context length the table cannot hold, a slot outside the pool) are
+ *    checked on the device: the access is skipped or clamped and a sticky bit
+ *    is set in the pool's status word, read back by pa_pool_check.
+ *
+ * Layouts (row-major, element = one 16-bit fp16 or bf16 value):
+ *   K pool, V pool   [num_blocks, num_kv_heads, block_size, head_dim]
+ *   new k, v         [num_tokens, num_kv_heads, head_dim]
+ *   q, out           [num_seqs, q_len, num_q_heads, head_dim]
+ *   block_tables     int32 [num_seqs, block_table_stride]
+ *   context_lens     int32 [num_seqs], counting the q_len newest tokens
+ *   slot_mapping     int64 [num_tokens], slot = block * block_size + offset
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or geometry; nothing launched */
+    PA_ERR_UNSUPPORTED = 2,    /* valid but not built (e.g. head_dim not in {64, 128}) */
+    PA_ERR_CUDA = 3,           /* a CUDA runtime or driver call failed */
+    PA_ERR_OOM = 4,            /* pa_pool_create could not allocate */
+    PA_ERR_DEVICE_BOUNDS = 5,  /* pa_pool_check: a kernel saw an out-of-range block id, slot or length */
+    PA_ERR_TIMEOUT = 6         /* pa_pool_check: a kernel gave up waiting on a copy (bounded wait) */
+} pa_status;
+
+typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef struct pa_pool pa_pool;
+
+/*
+ * Geometry of one KV pool and the limits the pool's workspace is sized for.
+ * A pool describes one attention layer's cache. Layers with the same geometry
+ * may share one pool object and pass their own caches to pa_cache_write and
+ * pa_decode.
+ */
+typedef struct pa_pool_config {
+    int32_t num_blocks;        /* physical blocks in the pool (> 0) */
+    int32_t block_size;        /* tokens per block: 16 or 32 */
+    int32_t num_kv_heads;      /* KV heads (> 0) */
+    int32_t head_dim;          /* 64 or 128 */
+    int32_t dtype;             /* pa_dtype of K, V, q and out */
+    int32_t device;            /* CUDA device ordinal */
+    int32_t partition_tokens;  /* context partition length for the split pass; 0 = 512.
+                                  Must be a positive multiple of block_size. */
+    int32_t max_seqs;          /* largest num_seqs passed to pa_decode */
+    int32_t max_q_heads;       /* largest num_q_heads */
+    int32_t max_q_len;         /* largest q_len (1..8) */
+    int32_t max_context_len;   /* largest context length (sizes the split workspace) */
+    void *k_cache;             /* device pointer to a caller-owned K pool, or NULL to allocate */
+    void *v_cache;             /* same for V */
+} pa_pool_config;
+
+/*
+ * Create a pool: validates the geometry, allocates the caches when the config
+ * passes NULL (left uninitialised), the split workspace and the status word on
+ * `device`. On success *out owns them until pa_destroy.
+ * Errors: PA_ERR_INVALID_ARG (geometry), PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_CUDA.
+ */
+pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out);
+
+/* Release everything the pool allocated (not caller-owned caches). NULL is a no-op. */
+void pa_destroy(pa_pool *pool);
+
+/* The pool's own K and V caches (device pointers; the ones passed in or allocated) and their bytes each. */
+pa_status pa_pool_caches(const pa_pool *pool, void **k_cache, void **v_cache, uint64_t *bytes_each);
+
+/*
+ * Cache write (scatter): for each token i with slot s = slot_mapping[i] >= 0
+ * and each KV head h, copy k[i][h][:] to K[s / block_size][h][s % block_size][:]
+ * and v likewise. Raw 16-bit words are copied without conversion; negative
+ * slots are skipped (padding). Slots beyond the pool are skipped and flagged
+ * (PA_ERR_DEVICE_BOUNDS). Two tokens with one slot: which one lands is unspecified.
+ * (A sequence growing past a block boundary receives a new physical block:
+ * yangyu.win blog #54, section 5 question 2.)
+ *   k, v            device, [num_tokens, num_kv_heads, head_dim]
+ *   slot_mapping    device, int64 [num_tokens]
+ *   k_cache/v_cache device pools to write, or NULL for the pool's own
+ */
+pa_status pa_cache_write(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
+                         int32_t num_tokens, void *k_cache, void *v_cache, void *stream);
+
+/*
+ * Paged attention decode. For sequence b, query row qi (0 <= qi < q_len) and
+ * query head h (KV head g = h / (num_q_heads / num_kv_heads)):
+ *   the row sits at position p = context_lens[b] - q_len + qi and attends to
+ *   tokens t = 0..p, token t read from physical block block_tables[b][t / bs]
+ *   at offset t % bs;
+ *   out[b][qi][h] = sum_t softmax_t(scale * q[b][qi][h] . K_t) * V_t
+ * (learn.tanhdev.com part 8: A_i = softmax(q_i K^T / sqrt(d_k)) computed block
+ * by block with an online softmax, o_i = sum_j sum_t a_{i,j,t} v_{(j,t)}).
+ * q_len > 1 verifies q_len speculative draft tokens in one pass with a causal
+ * mask (itimpress.au section 1; yangyu.win section 2.4). Several tables may
+ * name the same physical blocks (a shared copy-on-write prefix); no special
+ * case is needed. Contexts longer than the pool's partition_tokens are cut into
+ * partitions whose (max, sum, weighted V) are combined by a log-sum-exp merge
+ * (maths.nthquan ch. 17 "Scaling and deployment", section on sequence
+ * parallelism: local attention per segment, then a reduction); the merge uses
+ * the pool's workspace and a second kernel on the same stream.
+ * Accumulation is fp32; out is rounded to nearest even. Results are
+ * deterministic run to run. Concurrent pa_decode calls on one pool must be
+ * ordered (they share the workspace).
+ *   q                     device [num_seqs, q_len, num_q_heads, head_dim]
+ *   k_cache, v_cache      device pools, or NULL for the pool's own
+ *   block_tables          device int32 [num_seqs, block_table_stride]; entries at or
+ *                         beyond ceil(context_lens[b] / bs) are never read
+ *   context_lens          device int32 [num_seqs]; q_len <= context_lens[b] <= stride * bs
+ *   num_q_heads           a multiple of num_kv_heads; (num_q_heads / num_kv_heads) * q_len <= 32
+ *   scale                 softmax scale (1/sqrt(head_dim) in the pages' formula)
+ *   out                   device [num_seqs, q_len, num_q_heads, head_dim]
+ */
+pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale, void *out,
+                    void *stream);
+
+/*
+ * Synchronise the device, read and clear the pool's status word.
+ * Returns PA_OK, PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT or PA_ERR_CUDA.
+ */
+pa_status pa_pool_check(pa_pool *pool, void *stream);
+
+/* Number of kernels pa_decode launches for these arguments (1, or 2 with the merge); -1 on bad args. */
+int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t q_len);
+
+/* A static, human-readable name of a status code. */
+const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -173,6 +173,18 @@ int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, 
 
 /* --------------------------------------------------------- paged attention */
 
+/* Contiguous [L, d] copy of KV head g of one sequence through its block-table row. */
+static int gather_head(const uint16_t *pool, const int32_t *table_row, int64_t L, int64_t num_blocks, int bs,
+                       int Hkv, int d, int g, uint16_t *out) {
+    for (int64_t t = 0; t < L; ++t) {
+        int64_t phys = table_row[t / bs];
+        int64_t off = t % bs;
+        if (phys < 0 || phys >= num_blocks) return OR_ERR_BOUNDS;
+        memcpy(out + t * (int64_t)d, pool + ((phys * Hkv + g) * bs + off) * (int64_t)d, (size_t)d * sizeof(uint16_t));
+    }
+    return OR_OK;
+}
+
 typedef struct {
     const uint16_t *q, *k_pool, *v_pool;
     const int32_t *tables;
@@ -182,34 +194,59 @@ typedef struct {
     int nseq, q_len, Hq, Hkv, d, bs, dtype;
     float scale;
     double *out;
-    int next;                    /* work counter */
+    int next;                    /* work counter over (listed sequence, KV head) items */
     int err;
     pthread_mutex_t mu;
 } paged_job;
 
+/*
+ * One work item = one sequence and one KV head g: gather that head's K and V through the
+ * block table, then run attention for the G query heads of group g (the same computation
+ * as the whole-sequence call, restricted to one group: Hkv = 1, Hq = G).
+ */
 static void *paged_worker(void *arg) {
     paged_job *J = (paged_job *)arg;
+    const int G = J->Hq / J->Hkv;
     for (;;) {
         pthread_mutex_lock(&J->mu);
-        int i = J->next++;
+        int item = J->next++;
         pthread_mutex_unlock(&J->mu);
-        if (i >= J->nseq) break;
+        if (item >= J->nseq * J->Hkv) break;
+        int i = item / J->Hkv, g = item % J->Hkv;
         int b = J->seqs ? J->seqs[i] : i;
         int64_t L = J->lens[b];
-        size_t n = (size_t)L * J->Hkv * J->d;
-        uint16_t *kc = (uint16_t *)malloc(n * sizeof(uint16_t));
-        uint16_t *vc = (uint16_t *)malloc(n * sizeof(uint16_t));
-        int rc = (!kc || !vc) ? OR_ERR_OOM : OR_OK;
+        int rc = OR_OK;
+        if (L < J->q_len || (L + J->bs - 1) / J->bs > J->stride) rc = OR_ERR_BOUNDS;
+        uint16_t *kc = NULL, *vc = NULL, *qs = NULL;
+        double *os = NULL;
+        if (rc == OR_OK) {
+            kc = (uint16_t *)malloc((size_t)L * J->d * sizeof(uint16_t));
+            vc = (uint16_t *)malloc((size_t)L * J->d * sizeof(uint16_t));
+            qs = (uint16_t *)malloc((size_t)J->q_len * G * J->d * sizeof(uint16_t));
+            os = (double *)malloc((size_t)J->q_len * G * J->d * sizeof(double));
+            if (!kc || !vc || !qs || !os) rc = OR_ERR_OOM;
+        }
         const int32_t *row = J->tables + (int64_t)b * J->stride;
-        if (rc == OR_OK && (L + J->bs - 1) / J->bs > J->stride) rc = OR_ERR_BOUNDS;
-        if (rc == OR_OK) rc = oracle_gather(J->k_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, kc);
-        if (rc == OR_OK) rc = oracle_gather(J->v_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, vc);
+        if (rc == OR_OK) rc = gather_head(J->k_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, g, kc);
+        if (rc == OR_OK) rc = gather_head(J->v_pool, row, L, J->num_blocks, J->bs, J->Hkv, J->d, g, vc);
+        const uint16_t *qb = J->q + (int64_t)i * J->q_len * J->Hq * J->d;
+        double *ob = J->out + (int64_t)i * J->q_len * J->Hq * J->d;
+        if (rc == OR_OK) {
+            for (int qi = 0; qi < J->q_len; ++qi)
+                for (int hh = 0; hh < G; ++hh)
+                    memcpy(qs + ((int64_t)qi * G + hh) * J->d, qb + ((int64_t)qi * J->Hq + g * G + hh) * J->d,
+                           (size_t)J->d * sizeof(uint16_t));
+            rc = oracle_attention(qs, kc, vc, L, J->q_len, G, 1, J->d, J->dtype, J->scale, os, NULL);
+        }
         if (rc == OR_OK)
-            rc = oracle_attention(J->q + (int64_t)i * J->q_len * J->Hq * J->d, kc, vc, L, J->q_len, J->Hq,
-                                  J->Hkv, J->d, J->dtype, J->scale,
-                                  J->out + (int64_t)i * J->q_len * J->Hq * J->d, NULL);
+            for (int qi = 0; qi < J->q_len; ++qi)
+                for (int hh = 0; hh < G; ++hh)
+                    memcpy(ob + ((int64_t)qi * J->Hq + g * G + hh) * J->d, os + ((int64_t)qi * G + hh) * J->d,
+                           (size_t)J->d * sizeof(double));
         free(kc);
         free(vc);
+        free(qs);
+        free(os);
         if (rc != OR_OK) {
             pthread_mutex_lock(&J->mu);
             if (!J->err) J->err = rc;
@@ -228,22 +265,25 @@ int oracle_num_cpus(void) {
  * Paged decode for the sequences listed in seqs (or all num_seqs when seqs is NULL):
  * gather each sequence through its block-table row, then attention.
  *   q, out: one [q_len, Hq, d] row per listed sequence, in list order.
- *   Returns the number of threads used through *threads_used (may be NULL).
+ *   *threads_used (may be NULL) receives the number of threads used.
  */
 int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
                            const int32_t *block_tables, int64_t stride, const int32_t *context_lens,
                            const int32_t *seqs, int nseq, int64_t num_blocks, int bs, int q_len, int Hq,
                            int Hkv, int d, int dtype, float scale, double *out, int num_threads,
                            int *threads_used) {
-    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || nseq < 0) return OR_ERR_ARG;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || nseq < 0 || Hkv <= 0 ||
+        Hq % Hkv != 0 || bs <= 0)
+        return OR_ERR_ARG;
     paged_job J;
     memset(&J, 0, sizeof J);
     J.q = q; J.k_pool = k_pool; J.v_pool = v_pool; J.tables = block_tables; J.lens = context_lens;
     J.seqs = seqs; J.stride = stride; J.num_blocks = num_blocks; J.nseq = nseq; J.q_len = q_len;
     J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.bs = bs; J.dtype = dtype; J.scale = scale; J.out = out;
     pthread_mutex_init(&J.mu, NULL);
+    int items = nseq * Hkv;
     int nt = num_threads > 0 ? num_threads : oracle_num_cpus();
-    if (nt > nseq) nt = nseq > 0 ? nseq : 1;
+    if (nt > items) nt = items > 0 ? items : 1;
     pthread_t *th = (pthread_t *)malloc((size_t)nt * sizeof(pthread_t));
     if (!th) return OR_ERR_OOM;
     for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, paged_worker, &J);

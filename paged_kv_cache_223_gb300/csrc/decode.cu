@@ -1,0 +1,475 @@
+// decode.cu -- paged-attention decode / causal verify over a block-table-mapped KV pool,
+// plus the log-sum-exp merge of context partitions.
+//
+// What is computed (learn.tanhdev.com "Part 8: Inference optimization with vLLM",
+// section on executing the kernel math in CUDA): for query row i,
+//   A_{i,j} = q_i K_(j)^T / sqrt(d_k) block by block, an online softmax across blocks,
+//   o_i = sum_j sum_t a_{i,j,t} v_(j,t).
+// K_(j) is the j-th logical block of the sequence, found at physical block
+// block_table[b][j] (itimpress.au section 1; yangyu.win blog #54 section 2.2).
+//
+// Work decomposition. One CTA handles one (sequence b, KV head g, context
+// partition p). All q_len * G query rows that read KV head g (GQA groups;
+// q_len > 1 for verifying draft tokens) are handled together, so every K/V byte
+// of the partition is read from HBM once. The partition's tokens are cut into
+// 16-token tiles, dealt round-robin to the CTA's 4 warps. Each warp runs its own
+// STAGES-deep pipeline: its lane 0 issues TMA tile loads (128-byte swizzle, so
+// the ldmatrix reads below are bank-conflict free) completing on a per-stage
+// mbarrier, and the warp consumes tiles in order.
+//
+// Per tile the contraction is a small dense one, done on the tensor cores with
+// the keys as the M dimension (swap-AB): S^T[16 keys x 8*NT rows] = K_tile . Q^T,
+// then the fp32 online softmax per query row (column), then
+// O^T[D x 8*NT] += V_tile^T . P^T, where P^T comes out of the S^T accumulator
+// with one movmatrix per 8x8 block. The query rows fill the N dimension (8 per
+// MMA), so G = 8 heads use every column.
+//
+// Partitions (maths.nthquan ch. 17 "Scaling and deployment", section on sequence
+// parallelism: local attention per segment, then a reduction): a CTA whose
+// sequence has one partition writes the normalised output; otherwise it writes
+// (unnormalised O, running max, sum) and merge_kernel combines the partitions.
+#include <type_traits>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int STAGES = 3;
+
+__host__ __device__ constexpr int ring_bytes(int D) { return DECODE_WARPS * STAGES * 2 * TILE_TOKENS * D * 2; }
+__host__ __device__ constexpr int merge_bytes(int D, int nt) {
+    return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4;
+}
+__host__ __device__ constexpr int body_bytes(int D, int nt) {
+    return ring_bytes(D) > merge_bytes(D, nt) ? ring_bytes(D) : merge_bytes(D, nt);
+}
+
+static size_t smem_bytes(int D, int nt, int table_entries) {
+    return 1024 /* alignment slack */ + (size_t)body_bytes(D, nt) + DECODE_WARPS * STAGES * 8 +
+           (size_t)table_entries * 4;
+}
+
+size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt, 0); }
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeParams p) {
+    constexpr int HALVES = D / 64;                     // 128-byte swizzle spans per key row
+    constexpr int HALF_BYTES = TILE_TOKENS * 128;      // one span of a 16-row tile
+    constexpr int TILE_BYTES = TILE_TOKENS * D * 2;    // K (or V) of one tile
+    constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    constexpr int KSTEPS = D / 16;
+    constexpr int MT = D / 16;                         // m16 tiles of the head dimension (P.V)
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base_u32 - raw_u32);
+    const uint32_t bars_u32 = base_u32 + body_bytes(D, NT);
+    int *tbl = reinterpret_cast<int *>(smem + body_bytes(D, NT) + DECODE_WARPS * STAGES * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = blockIdx.x % p.max_parts;
+    const int bg = blockIdx.x / p.max_parts;
+    const int g = bg % p.Hkv;
+    const int b = bg / p.Hkv;
+
+    // ---- context of this sequence, clamped to what the table / launch can hold
+    int L = __ldg(p.context_lens + b);
+    if (L < p.q_len || L > p.max_ctx) {
+        if (threadIdx.x == 0 && part == 0) set_status(p.status, STATUS_BOUNDS);
+        L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+    }
+    const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
+    if (part >= nparts) return;
+    const int t_begin = part * p.part_tokens;
+    const int ntok = min(p.part_tokens, L - t_begin);
+    const int ntiles = (ntok + TILE_TOKENS - 1) / TILE_TOKENS;
+    const int blk0 = t_begin / p.bs;
+    const int nblk = (ntok + p.bs - 1) / p.bs;
+
+    // ---- this partition's block ids (block-table gather), validated
+    const int32_t *trow = p.block_tables + (int64_t)b * p.stride + blk0;
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
+        int id = __ldg(trow + i);
+        if (id < 0 || id >= p.num_blocks) {
+            set_status(p.status, STATUS_BOUNDS);
+            id = 0;
+        }
+        tbl[i] = id;
+    }
+    if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(bars_u32 + (warp * STAGES + s) * 8, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int my_tiles = ntiles > warp ? (ntiles - warp + DECODE_WARPS - 1) / DECODE_WARPS : 0;
+    const uint32_t ring_u32 = base_u32 + warp * STAGES * STAGE_BYTES;
+    const uint64_t policy = l2_policy_evict_first();
+
+    auto issue = [&](int it) {
+        const int i = warp + it * DECODE_WARPS;          // tile index within the partition
+        const int s = it % STAGES;
+        const int tok = i * TILE_TOKENS;                 // token offset within the partition
+        const int row0 = (tbl[tok / p.bs] * p.Hkv + g) * p.bs + (tok % p.bs);
+        const uint32_t bar = bars_u32 + (warp * STAGES + s) * 8;
+        const uint32_t kdst = ring_u32 + s * STAGE_BYTES;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            tma_load_2d(kdst + h * HALF_BYTES, &tmk, h * 64, row0, bar, policy);
+            tma_load_2d(kdst + TILE_BYTES + h * HALF_BYTES, &tmv, h * 64, row0, bar, policy);
+        }
+    };
+
+    int issued = 0;
+    if (lane == 0) {
+        const int n0 = my_tiles < STAGES ? my_tiles : STAGES;
+        for (int it = 0; it < n0; ++it) issue(it);
+    }
+    issued = my_tiles < STAGES ? my_tiles : STAGES;
+
+    // ---- query fragments: B operand (col-major 16 x 8) of S^T = K . Q^T
+    const int gq = lane >> 2;   // MMA group id: key row within an 8-row half; query column for B
+    const int tq = lane & 3;    // thread in group
+    uint32_t qf[NT][KSTEPS][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int r = nt * 8 + gq;
+        if (r < p.rows) {
+            const int qi = r / p.G, hh = r - (r / p.G) * p.G;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                reinterpret_cast<const T *>(p.q) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * D);
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                qf[nt][ks][0] = __ldg(qrow + ks * 8 + tq);
+                qf[nt][ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
+        }
+    }
+    // causal limit (inclusive) of the query columns this thread accumulates
+    int lim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            int r = nt * 8 + 2 * tq + j;
+            int qi = r / p.G;
+            if (qi > p.q_len - 1) qi = p.q_len - 1;
+            lim[nt][j] = L - p.q_len + qi;
+        }
+
+    float m[NT][2], l[NT][2], o[MT][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int md = 0; md < MT; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
+    }
+
+    bool ok = true;
+    int it = 0;
+    for (; it < my_tiles; ++it) {
+        const int s = it % STAGES;
+        if (!mbar_wait_bounded(bars_u32 + (warp * STAGES + s) * 8, (uint32_t)(it / STAGES) & 1u, p.wait_ns)) {
+            ok = false;
+            break;
+        }
+        const int i = warp + it * DECODE_WARPS;
+        const int tile_t0 = t_begin + i * TILE_TOKENS;   // absolute token index of the tile's first row
+        const uint32_t kb = ring_u32 + s * STAGE_BYTES;
+        const uint32_t vb = kb + TILE_BYTES;
+
+        // Rows past the context hold other data (possibly NaN): zero them in V so that
+        // 0-weight x row stays 0 in the P.V product. Scores of those rows are masked below.
+        const int nvalid = L - tile_t0;
+        if (nvalid < TILE_TOKENS) {
+            const int nz = (TILE_TOKENS - nvalid) * 8;   // 16-byte chunks per span
+            uint8_t *vgen = smem + (vb - base_u32);
+            for (int c = lane; c < nz * HALVES; c += 32) {
+                const int h = c / nz, rc = c - (c / nz) * nz;
+                *reinterpret_cast<uint4 *>(vgen + h * HALF_BYTES + (nvalid + rc / 8) * 128 + (rc % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // S^T = K . Q^T (16 keys x 8*NT query columns)
+        float sacc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+        {
+            const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                const int chunk = ks * 2 + (lane >> 4);
+                const uint32_t addr = kb + (chunk >> 3) * HALF_BYTES + krow * 128 + (((chunk & 7) ^ (krow & 7)) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816<T>(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+            }
+        }
+
+        // online softmax per query column (log2 domain)
+        const int t_lo = tile_t0 + gq, t_hi = t_lo + 8;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float s0 = t_lo <= lim[nt][j] ? sacc[nt][j] * p.scale_log2 : -INFINITY;
+                const float s1 = t_hi <= lim[nt][j] ? sacc[nt][2 + j] * p.scale_log2 : -INFINITY;
+                float mx = fmaxf(s0, s1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mnew = fmaxf(m[nt][j], mx);
+                const float muse = mnew == -INFINITY ? 0.f : mnew;
+                const float alpha = exp2f(m[nt][j] - muse);
+                const float p0 = exp2f(s0 - muse), p1 = exp2f(s1 - muse);
+                l[nt][j] = l[nt][j] * alpha + p0 + p1;
+                m[nt][j] = mnew;
+                sacc[nt][j] = p0;
+                sacc[nt][2 + j] = p1;
+#pragma unroll
+                for (int md = 0; md < MT; ++md) {
+                    o[md][nt][j] *= alpha;
+                    o[md][nt][2 + j] *= alpha;
+                }
+            }
+
+        // P^T as the B operand (16 keys x 8 columns): transpose the two 8x8 halves of S^T
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movmatrix_trans(pack2<T>(sacc[nt][0], sacc[nt][1]));
+            pb[nt][1] = movmatrix_trans(pack2<T>(sacc[nt][2], sacc[nt][3]));
+        }
+
+        // O^T += V^T . P^T
+        {
+            const int vrow = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+            for (int md = 0; md < MT; ++md) {
+                const int chunk = md * 2 + ((lane >> 3) & 1);
+                const uint32_t addr = vb + (chunk >> 3) * HALF_BYTES + vrow * 128 + (((chunk & 7) ^ (vrow & 7)) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(addr, a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816<T>(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+        }
+        __syncwarp();
+        if (it + STAGES < my_tiles) {
+            if (lane == 0) issue(it + STAGES);
+            ++issued;
+        }
+    }
+
+    // full row sums of this warp (the 8 lanes sharing a column hold disjoint keys)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v = l[nt][j];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            l[nt][j] = v;
+        }
+
+    if (__syncthreads_or(!ok)) {
+        // A copy did not arrive in time: record it, wait (bounded) for this warp's copies still in
+        // flight so none lands after the CTA exits, and leave without writing results.
+        if (threadIdx.x == 0) set_status(p.status, STATUS_TIMEOUT);
+        if (lane == 0)
+            for (int k = it; k < issued; ++k)
+                mbar_wait_bounded(bars_u32 + (warp * STAGES + (k % STAGES)) * 8, (uint32_t)(k / STAGES) & 1u,
+                                  p.wait_ns);
+        return;
+    }
+
+    // ---- combine the 4 warps (smem; the tile ring is free now)
+    constexpr int RP = NT * 8;
+    constexpr int OSTR = D + 4;   // padded row: the fragment stores below hit 32 distinct banks
+    float *ow = reinterpret_cast<float *>(smem);
+    float *mlw = ow + DECODE_WARPS * RP * OSTR;
+#pragma unroll
+    for (int md = 0; md < MT; ++md)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int dim = md * 16 + gq + (e >> 1) * 8;
+                const int col = nt * 8 + 2 * tq + (e & 1);
+                ow[(warp * RP + col) * OSTR + dim] = o[md][nt][e];
+            }
+    if (gq == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = nt * 8 + 2 * tq + j;
+                mlw[(warp * RP + col) * 2] = m[nt][j];
+                mlw[(warp * RP + col) * 2 + 1] = l[nt][j];
+            }
+    }
+    __syncthreads();
+
+    const bool direct = nparts == 1;
+    for (int idx = threadIdx.x; idx < p.rows * (D / 2); idx += blockDim.x) {
+        const int r = idx / (D / 2);
+        const int dp = (idx - r * (D / 2)) * 2;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < DECODE_WARPS; ++w) M = fmaxf(M, mlw[(w * RP + r) * 2]);
+        const float Muse = M == -INFINITY ? 0.f : M;
+        float o0 = 0.f, o1 = 0.f, ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < DECODE_WARPS; ++w) {
+            const float sc = exp2f(mlw[(w * RP + r) * 2] - Muse);
+            const float2 ov = *reinterpret_cast<const float2 *>(ow + (w * RP + r) * OSTR + dp);
+            o0 += sc * ov.x;
+            o1 += sc * ov.y;
+            ls += sc * mlw[(w * RP + r) * 2 + 1];
+        }
+        const int qi = r / p.G;
+        const int h = g * p.G + (r - qi * p.G);
+        const int64_t orow = ((int64_t)b * p.q_len + qi) * p.Hq + h;
+        if (direct) {
+            *reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.out) + orow * D + dp) = pack2<T>(o0 / ls, o1 / ls);
+        } else {
+            const int64_t prow = orow * p.max_parts + part;
+            *reinterpret_cast<float2 *>(p.part_o + prow * D + dp) = make_float2(o0, o1);
+            if (dp == 0) p.part_ml[prow] = make_float2(M, ls);
+        }
+    }
+}
+
+// Log-sum-exp merge of the partitions of one output row (b, qi, h):
+//   M = max_p m_p,  out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p
+// Warp w folds partitions w, w+4, ... in order; the four results are folded in warp order,
+// so the result does not depend on timing.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
+    constexpr int VPL = D / 32;   // values per lane
+    __shared__ float s_o[4][D];
+    __shared__ float s_ml[4][2];
+    const int row = blockIdx.x;
+    const int b = row / (p.q_len * p.Hq);
+    int L = __ldg(p.context_lens + b);
+    L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+    const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
+    if (nparts <= 1) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float M = -INFINITY, ls = 0.f, acc[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
+    const float2 *ml = p.part_ml + (int64_t)row * p.max_parts;
+    const float *po = p.part_o + (int64_t)row * p.max_parts * D;
+    for (int pp = warp; pp < nparts; pp += 4) {
+        const float2 v = ml[pp];
+        if (!(v.y > 0.f)) continue;
+        const float Mn = fmaxf(M, v.x);
+        const float a = exp2f(M - Mn);
+        const float c = exp2f(v.x - Mn);
+        ls = ls * a + v.y * c;
+        const float *src = po + (int64_t)pp * D + lane * VPL;
+        if (VPL == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src);
+            acc[0] = acc[0] * a + c * x.x;
+            acc[1] = acc[1] * a + c * x.y;
+            acc[2] = acc[2] * a + c * x.z;
+            acc[3] = acc[3] * a + c * x.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) acc[k] = acc[k] * a + c * src[k];
+        }
+        M = Mn;
+    }
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) s_o[warp][lane * VPL + k] = acc[k];
+    if (lane == 0) {
+        s_ml[warp][0] = M;
+        s_ml[warp][1] = ls;
+    }
+    __syncthreads();
+    for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
+        float Mt = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) Mt = fmaxf(Mt, s_ml[w][0]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float sc = s_ml[w][0] == -INFINITY ? 0.f : exp2f(s_ml[w][0] - Mt);
+            num += sc * s_o[w][dim];
+            den += sc * s_ml[w][1];
+        }
+        const float r = num / den;
+        T *out = reinterpret_cast<T *>(p.out) + (int64_t)row * D + dim;
+        if constexpr (std::is_same<T, __half>::value)
+            *out = __float2half_rn(r);
+        else
+            *out = __float2bfloat16_rn(r);
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <typename T, int D, int NT>
+static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t stream) {
+    const size_t smem = smem_bytes(D, NT, (p.part_tokens + p.bs - 1) / p.bs);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)p.num_seqs * p.Hkv * p.max_parts;
+    decode_kernel<T, D, NT><<<(unsigned)grid, DECODE_WARPS * 32, smem, stream>>>(tmk, tmv, p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_decode_d(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t stream) {
+    switch ((p.rows + 7) / 8) {
+        case 1: return launch_decode_t<T, D, 1>(p, tmk, tmv, stream);
+        case 2: return launch_decode_t<T, D, 2>(p, tmk, tmv, stream);
+        case 3: return launch_decode_t<T, D, 3>(p, tmk, tmv, stream);
+        case 4: return launch_decode_t<T, D, 4>(p, tmk, tmv, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
+                          const CUtensorMap &tmv, cudaStream_t stream) {
+    if (dtype == PA_FP16) {
+        if (head_dim == 128) return launch_decode_d<__half, 128>(p, tmk, tmv, stream);
+        if (head_dim == 64) return launch_decode_d<__half, 64>(p, tmk, tmv, stream);
+    } else {
+        if (head_dim == 128) return launch_decode_d<__nv_bfloat16, 128>(p, tmk, tmv, stream);
+        if (head_dim == 64) return launch_decode_d<__nv_bfloat16, 64>(p, tmk, tmv, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.num_seqs * p.q_len * p.Hq;
+    if (dtype == PA_FP16) {
+        if (head_dim == 128) merge_kernel<__half, 128><<<(unsigned)rows, 128, 0, stream>>>(p);
+        else merge_kernel<__half, 64><<<(unsigned)rows, 128, 0, stream>>>(p);
+    } else {
+        if (head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<(unsigned)rows, 128, 0, stream>>>(p);
+        else merge_kernel<__nv_bfloat16, 64><<<(unsigned)rows, 128, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,306 @@
+// pa_api.cu -- the C ABI declared in include/pagedattn.h: pool lifecycle, argument
+// validation, TMA descriptor encoding and kernel launches. No computation happens
+// here; every step of the path runs in the kernels of cache_write.cu and decode.cu.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+#include <unordered_map>
+
+#include "pa_internal.h"
+
+using namespace pa;
+
+struct pa_pool {
+    pa_pool_config cfg;
+    void *k_cache = nullptr;
+    void *v_cache = nullptr;
+    bool owns_caches = false;
+    uint64_t cache_bytes = 0;
+    float *part_o = nullptr;
+    float2 *part_ml = nullptr;
+    int64_t ws_slots = 0;        // (output row, partition) pairs the workspace holds
+    int *status = nullptr;
+    int sm_count = 0;
+    int part_tokens = 512;
+    uint64_t wait_ns = 2000000000ull;
+    std::mutex mu;
+    std::unordered_map<const void *, CUtensorMap> maps;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool seen as a 2-D tensor: rows = num_blocks * Hkv * block_size key rows of head_dim
+// elements. Boxes are 16 rows x 64 elements (128 bytes), swizzled 128B in shared memory.
+pa_status tensor_map(pa_pool *pool, const void *cache, CUtensorMap *out) {
+    std::lock_guard<std::mutex> lk(pool->mu);
+    auto it = pool->maps.find(cache);
+    if (it != pool->maps.end()) {
+        *out = it->second;
+        return PA_OK;
+    }
+    auto fn = encode_fn();
+    if (!fn) return PA_ERR_CUDA;
+    const pa_pool_config &c = pool->cfg;
+    CUtensorMap m;
+    cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)TILE_TOKENS};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&m, c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
+    if (pool->maps.size() > 4096) pool->maps.clear();
+    pool->maps.emplace(cache, m);
+    *out = m;
+    return PA_OK;
+}
+
+void free_pool(pa_pool *p) {
+    if (!p) return;
+    DeviceGuard g(p->cfg.device);
+    if (p->owns_caches) {
+        cudaFree(p->k_cache);
+        cudaFree(p->v_cache);
+    }
+    cudaFree(p->part_o);
+    cudaFree(p->part_ml);
+    cudaFree(p->status);
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_OOM: return "out of device memory";
+        case PA_ERR_DEVICE_BOUNDS: return "device saw an out-of-range block id, slot or context length";
+        case PA_ERR_TIMEOUT: return "device gave up waiting on a copy";
+    }
+    return "unknown status";
+}
+
+pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out) {
+    if (!config || !out) return PA_ERR_INVALID_ARG;
+    *out = nullptr;
+    pa_pool_config c = *config;
+    if (c.num_blocks <= 0 || c.num_kv_heads <= 0 || c.max_seqs <= 0 || c.max_q_heads <= 0 || c.max_q_len < 1 ||
+        c.max_q_len > 8 || c.max_context_len < 1 || c.device < 0)
+        return PA_ERR_INVALID_ARG;
+    if (c.block_size != 16 && c.block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (c.head_dim != 64 && c.head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (c.dtype != PA_FP16 && c.dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (c.partition_tokens == 0) c.partition_tokens = 512;
+    if (c.partition_tokens < 0 || c.partition_tokens % c.block_size != 0 || c.partition_tokens > 16384)
+        return PA_ERR_INVALID_ARG;
+    if ((c.k_cache == nullptr) != (c.v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    if ((c.k_cache && !aligned16(c.k_cache)) || (c.v_cache && !aligned16(c.v_cache))) return PA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)c.num_blocks * c.num_kv_heads * c.block_size;
+    if (rows >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
+
+    DeviceGuard g(c.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    pa_pool *p = new pa_pool();
+    p->cfg = c;
+    p->part_tokens = c.partition_tokens;
+    p->cache_bytes = (uint64_t)rows * c.head_dim * 2;
+    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess) {
+        delete p;
+        return PA_ERR_CUDA;
+    }
+    if (c.k_cache) {
+        p->k_cache = c.k_cache;
+        p->v_cache = c.v_cache;
+    } else {
+        p->owns_caches = true;
+        if (cudaMalloc(&p->k_cache, p->cache_bytes) != cudaSuccess ||
+            cudaMalloc(&p->v_cache, p->cache_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            free_pool(p);
+            return PA_ERR_OOM;
+        }
+    }
+    const int64_t max_parts = (c.max_context_len + c.partition_tokens - 1) / c.partition_tokens;
+    p->ws_slots = (int64_t)c.max_seqs * c.max_q_len * c.max_q_heads * max_parts;
+    if (max_parts > 1) {
+        if (cudaMalloc(&p->part_o, (size_t)p->ws_slots * c.head_dim * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&p->part_ml, (size_t)p->ws_slots * sizeof(float2)) != cudaSuccess) {
+            cudaGetLastError();
+            free_pool(p);
+            return PA_ERR_OOM;
+        }
+    }
+    if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess || cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        free_pool(p);
+        return PA_ERR_OOM;
+    }
+    *out = p;
+    return PA_OK;
+}
+
+void pa_destroy(pa_pool *pool) { free_pool(pool); }
+
+pa_status pa_pool_caches(const pa_pool *pool, void **k_cache, void **v_cache, uint64_t *bytes_each) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    if (k_cache) *k_cache = pool->k_cache;
+    if (v_cache) *v_cache = pool->v_cache;
+    if (bytes_each) *bytes_each = pool->cache_bytes;
+    return PA_OK;
+}
+
+pa_status pa_cache_write(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
+                         int32_t num_tokens, void *k_cache, void *v_cache, void *stream) {
+    if (!pool || num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    if (!k_cache) {
+        k_cache = pool->k_cache;
+        v_cache = pool->v_cache;
+    }
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    const pa_pool_config &c = pool->cfg;
+    DeviceGuard g(c.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    CacheWriteParams p;
+    p.k = static_cast<const uint4 *>(k);
+    p.v = static_cast<const uint4 *>(v);
+    p.slots = slot_mapping;
+    p.k_cache = static_cast<uint4 *>(k_cache);
+    p.v_cache = static_cast<uint4 *>(v_cache);
+    p.status = pool->status;
+    p.num_tokens = num_tokens;
+    p.Hkv = c.num_kv_heads;
+    p.vec_per_row = c.head_dim / 8;
+    p.bs = c.block_size;
+    p.num_blocks = c.num_blocks;
+    return launch_cache_write(p, pool->sm_count, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                                     : PA_ERR_CUDA;
+}
+
+static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t q_len, DecodeParams &p) {
+    const pa_pool_config &c = pool->cfg;
+    if (stride < 1 || num_seqs < 1 || num_seqs > c.max_seqs || num_q_heads < 1 || num_q_heads > c.max_q_heads ||
+        num_q_heads % c.num_kv_heads != 0 || q_len < 1 || q_len > c.max_q_len)
+        return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / c.num_kv_heads;
+    if (G * q_len > MAX_ROWS) return PA_ERR_UNSUPPORTED;
+    int64_t max_ctx = (int64_t)stride * c.block_size;
+    if (max_ctx > c.max_context_len) max_ctx = c.max_context_len;
+    const int64_t max_parts = (max_ctx + pool->part_tokens - 1) / pool->part_tokens;
+    if (max_parts > 1 && (int64_t)num_seqs * q_len * num_q_heads * max_parts > pool->ws_slots) return PA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * c.num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    p.stride = stride;
+    p.num_seqs = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = c.num_kv_heads;
+    p.G = G;
+    p.q_len = q_len;
+    p.rows = G * q_len;
+    p.bs = c.block_size;
+    p.num_blocks = c.num_blocks;
+    p.part_tokens = pool->part_tokens;
+    p.max_parts = (int)max_parts;
+    p.max_ctx = (int)max_ctx;
+    p.wait_ns = pool->wait_ns;
+    p.part_o = pool->part_o;
+    p.part_ml = pool->part_ml;
+    p.status = pool->status;
+    return PA_OK;
+}
+
+int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t q_len) {
+    if (!pool) return -1;
+    DecodeParams p;
+    if (decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p) != PA_OK) return -1;
+    return p.max_parts > 1 ? 2 : 1;
+}
+
+pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale, void *out, void *stream) {
+    if (!pool || !q || !out || !block_tables || !context_lens || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    if (!k_cache) {
+        k_cache = pool->k_cache;
+        v_cache = pool->v_cache;
+    }
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams p;
+    pa_status st = decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p);
+    if (st != PA_OK) return st;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    DeviceGuard g(pool->cfg.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    CUtensorMap tmk, tmv;
+    if ((st = tensor_map(pool, k_cache, &tmk)) != PA_OK) return st;
+    if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+pa_status pa_pool_check(pa_pool *pool, void *stream) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    DeviceGuard g(pool->cfg.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaMemcpyAsync(&h, pool->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess || cudaMemsetAsync(pool->status, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (h & STATUS_TIMEOUT) return PA_ERR_TIMEOUT;
+    if (h & STATUS_BOUNDS) return PA_ERR_DEVICE_BOUNDS;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// pa_internal.h -- types shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Bits of the device status word (read by pa_pool_check).
+constexpr int STATUS_BOUNDS = 1;   // block id, slot or context length outside what the pool/table holds
+constexpr int STATUS_TIMEOUT = 2;  // a bounded wait on a TMA copy ran out
+
+constexpr int TILE_TOKENS = 16;    // tokens per staged K/V tile (one m16 MMA tile of keys)
+constexpr int DECODE_WARPS = 4;    // warps per decode CTA (each runs its own copy pipeline)
+constexpr int MAX_ROWS = 32;       // query rows per (sequence, KV head): q_len * (Hq / Hkv)
+
+struct DecodeParams {
+    const void *q;
+    void *out;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *part_o;       // [num_seqs, q_len, Hq, max_parts, D] unnormalised partition outputs
+    float2 *part_ml;     // [num_seqs, q_len, Hq, max_parts] (running max in log2 units, sum)
+    int *status;
+    int64_t stride;      // block-table row stride (entries)
+    int num_seqs;
+    int Hq;
+    int Hkv;
+    int G;               // Hq / Hkv
+    int q_len;
+    int rows;            // q_len * G
+    int bs;              // block size (16 or 32)
+    int num_blocks;
+    int part_tokens;     // partition length (multiple of bs)
+    int max_parts;       // partitions launched per (sequence, KV head)
+    int max_ctx;         // longest context the launch covers (max_parts * part_tokens, <= stride * bs)
+    float scale_log2;    // scale * log2(e)
+    uint64_t wait_ns;    // bounded-wait limit
+};
+
+struct CacheWriteParams {
+    const uint4 *k;
+    const uint4 *v;
+    const int64_t *slots;
+    uint4 *k_cache;
+    uint4 *v_cache;
+    int *status;
+    int64_t num_tokens;
+    int Hkv;
+    int vec_per_row;     // head_dim / 8
+    int bs;
+    int64_t num_blocks;
+};
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_cache_write(const CacheWriteParams &p, int sm_count, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
+                          const CUtensorMap &tmv, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream);
+size_t decode_smem_bytes(int head_dim, int nt);
+
+}  // namespace pa

@@ -1,0 +1,180 @@
+"""Python binding of the C ABI in include/pagedattn.h (ctypes; argument marshalling only).
+
+Torch tensors provide device memory and streams; every step of the paged-attention path
+runs in the CUDA library. There is no fallback: if the library is missing this module
+raises on load.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OOM, PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT = range(7)
+PA_FP16, PA_BF16 = 0, 1
+_TORCH_DTYPE = {PA_FP16: torch.float16, PA_BF16: torch.bfloat16}
+_PA_DTYPE = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
+
+
+class PaPoolConfig(C.Structure):
+    _fields_ = [("num_blocks", C.c_int32), ("block_size", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("dtype", C.c_int32), ("device", C.c_int32),
+                ("partition_tokens", C.c_int32), ("max_seqs", C.c_int32), ("max_q_heads", C.c_int32),
+                ("max_q_len", C.c_int32), ("max_context_len", C.c_int32), ("k_cache", C.c_void_p),
+                ("v_cache", C.c_void_p)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libpagedattn.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                                   "(run `python -m paged_kv_cache_223_gb300._build`)")
+            L = C.CDLL(LIB_PATH)
+            P, I32, I64 = C.c_void_p, C.c_int32, C.c_int64
+            L.pa_pool_create.argtypes = [C.POINTER(PaPoolConfig), C.POINTER(C.c_void_p)]
+            L.pa_destroy.argtypes = [P]
+            L.pa_destroy.restype = None
+            L.pa_pool_caches.argtypes = [P, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.POINTER(C.c_uint64)]
+            L.pa_cache_write.argtypes = [P, P, P, P, I32, P, P, P]
+            L.pa_decode.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
+            L.pa_pool_check.argtypes = [P, P]
+            L.pa_decode_launches.argtypes = [P, I32, I32, I32, I32]
+            L.pa_decode_launches.restype = I32
+            L.pa_status_string.argtypes = [C.c_int]
+            L.pa_status_string.restype = C.c_char_p
+            for f in ("pa_pool_create", "pa_pool_caches", "pa_cache_write", "pa_decode", "pa_pool_check"):
+                getattr(L, f).restype = C.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    return (stream or torch.cuda.current_stream()).cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> torch.Tensor:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+class Pool:
+    """One paged KV pool (pa_pool_create) with its caches.
+
+    The caches are torch tensors [num_blocks, num_kv_heads, block_size, head_dim], created
+    here unless given; the pool only borrows them.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                 dtype: torch.dtype = torch.float16, device: int = 0, partition_tokens: int = 0,
+                 max_seqs: int = 256, max_q_heads: int = 64, max_q_len: int = 8, max_context_len: int = 8192,
+                 k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None):
+        self.geometry = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.dtype = dtype
+        self.device = torch.device("cuda", device)
+        if k_cache is None:
+            k_cache = torch.empty(self.geometry, dtype=dtype, device=self.device)
+            v_cache = torch.empty(self.geometry, dtype=dtype, device=self.device)
+        for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+            _dev(t, name, dtype)
+            if tuple(t.shape) != self.geometry:
+                raise ValueError(f"{name} must have shape {self.geometry}")
+        self.k_cache, self.v_cache = k_cache, v_cache
+        cfg = PaPoolConfig(num_blocks, block_size, num_kv_heads, head_dim, _PA_DTYPE[dtype], device,
+                           partition_tokens, max_seqs, max_q_heads, max_q_len, max_context_len,
+                           k_cache.data_ptr(), v_cache.data_ptr())
+        h = C.c_void_p()
+        _check(lib().pa_pool_create(C.byref(cfg), C.byref(h)), "pa_pool_create")
+        self._h = h
+
+    @property
+    def handle(self) -> C.c_void_p:
+        if self._h is None:
+            raise RuntimeError("pool is closed")
+        return self._h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None:
+            lib().pa_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def cache_write(self, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Scatter k, v [N, Hkv, d] into the slots given by slot_mapping (int64 [N]; -1 = skip)."""
+        _dev(k, "k", self.dtype), _dev(v, "v", self.dtype), _dev(slot_mapping, "slot_mapping", torch.int64)
+        _check(lib().pa_cache_write(self.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.numel(),
+                                    _ptr(k_cache), _ptr(v_cache), _stream(stream)), "pa_cache_write")
+
+    def decode(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+               out: Optional[torch.Tensor] = None, k_cache: Optional[torch.Tensor] = None,
+               v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Paged attention for q [B, q_len, Hq, d] -> out [B, q_len, Hq, d] (causal over the q_len rows)."""
+        _dev(q, "q", self.dtype)
+        _dev(block_tables, "block_tables", torch.int32)
+        _dev(context_lens, "context_lens", torch.int32)
+        B, q_len, Hq, d = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        _dev(out, "out", self.dtype)
+        _check(lib().pa_decode(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
+                               _stream(stream)), "pa_decode")
+        return out
+
+    def launches(self, block_table_stride: int, num_seqs: int, num_q_heads: int, q_len: int) -> int:
+        return lib().pa_decode_launches(self.handle, block_table_stride, num_seqs, num_q_heads, q_len)
+
+    def check(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Synchronise and return (and clear) the device status: PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_TIMEOUT."""
+        return lib().pa_pool_check(self.handle, _stream(stream))
+
+
+def pool_create_status(**cfg) -> int:
+    """pa_pool_create's status for a raw config (host-side validation; destroys the pool on success)."""
+    c = PaPoolConfig(**cfg)
+    h = C.c_void_p()
+    st = lib().pa_pool_create(C.byref(c), C.byref(h))
+    if st == PA_OK:
+        lib().pa_destroy(h)
+    return st

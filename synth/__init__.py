@@ -25,8 +25,11 @@ workloads too large to draw on the host; the two agree bit for bit.
 """
 from __future__ import annotations
 
+import ctypes
 import dataclasses
 import math
+import os
+import threading
 from typing import Dict, List, Optional, Tuple
 
 import numpy as np
@@ -98,6 +101,42 @@ def f32_to_bits16(x: np.ndarray, dtype: int) -> np.ndarray:
 
 def values16(seed: int, stream: int, idx, dtype: int, sigma: float = 1.0, mean: float = 0.0) -> np.ndarray:
     return f32_to_bits16(unit_f32(seed, stream, idx, sigma, mean), dtype)
+
+
+_HOST_LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libsynthhost.so")
+_host_lock = threading.Lock()
+_host = None
+
+
+def _host_lib():
+    """The C statement of the same recipe (synth/csrc/synth_host.c), multithreaded; None if not built."""
+    global _host
+    with _host_lock:
+        if _host is None:
+            if not os.path.exists(_HOST_LIB):
+                return None
+            L = ctypes.CDLL(_HOST_LIB)
+            L.synth_host_fill_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int, ctypes.c_float,
+                                               ctypes.c_float, ctypes.c_int]
+            L.synth_host_fill_rows.restype = ctypes.c_int
+            _host = L
+    return _host
+
+
+def fill_rows16(rows: Optional[np.ndarray], nrows: int, row_len: int, seed: int, stream: int, dtype: int,
+                sigma: float = 1.0, mean: float = 0.0, use_c: bool = True) -> np.ndarray:
+    """[nrows, row_len] words; row r holds counters rows[r]*row_len + c (rows None: r)."""
+    L = _host_lib() if use_c else None
+    if L is None:
+        r = np.arange(nrows, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+        idx = (r[:, None] * row_len + np.arange(row_len, dtype=np.int64)[None, :]).astype(np.uint64)
+        return values16(seed, stream, idx, dtype, sigma, mean)
+    out = np.empty((nrows, row_len), dtype=np.uint16)
+    rr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    L.synth_host_fill_rows(out.ctypes.data, None if rr is None else rr.ctypes.data, nrows, row_len,
+                           seed & MASK64, stream & MASK64, dtype, sigma, mean, os.cpu_count() or 1)
+    return out
 
 
 def uniform_int(seed: int, stream: int, n: int, lo: int, hi: int) -> np.ndarray:
@@ -184,7 +223,6 @@ class Workload:
         """16-bit words of K or V for tokens t of sequence b: shape [len(t), Hkv, d]."""
         is_pre, row = self.token_rows(b, t)
         HD = self.Hkv * self.d
-        col = np.arange(HD, dtype=np.int64)
         kind, pkind = (K_K, K_KP) if which == "k" else (K_V, K_VP)
         mean = self.v_mean if which == "v" else 0.0
         out = np.empty((len(row), HD), dtype=np.uint16)
@@ -192,16 +230,16 @@ class Workload:
             sel = is_pre == flag
             if not sel.any():
                 continue
-            idx = (row[sel][:, None] * HD + col[None, :]).astype(np.uint64)
-            out[sel] = values16(self.seed, self.stream(layer, kd), idx, self.dtype, 1.0, mean)
+            out[sel] = fill_rows16(row[sel], int(sel.sum()), HD, self.seed, self.stream(layer, kd), self.dtype,
+                                   1.0, mean)
         return out.reshape(len(row), self.Hkv, self.d)
 
     def q_values(self, layer: int, seqs: Optional[np.ndarray] = None) -> np.ndarray:
         """16-bit words of q for sequences `seqs` (default all): [len(seqs), q_len, Hq, d]."""
         seqs = np.arange(self.B) if seqs is None else np.asarray(seqs)
         per = self.q_len * self.Hq * self.d
-        idx = (seqs[:, None].astype(np.int64) * per + np.arange(per)[None, :]).astype(np.uint64)
-        w = values16(self.seed, self.stream(layer, K_Q), idx, self.dtype, self.q_sigma, 0.0)
+        w = fill_rows16(seqs.astype(np.int64), len(seqs), per, self.seed, self.stream(layer, K_Q), self.dtype,
+                        self.q_sigma, 0.0)
         return w.reshape(len(seqs), self.q_len, self.Hq, self.d)
 
     # ---- cache-write plans ----------------------------------------------------------
@@ -314,6 +352,23 @@ def workload(k: int, layers: Optional[int] = None, batch: Optional[int] = None,
                   dtype=dt, context_lens=lens, num_blocks=NB, block_tables=tables, layers=nl,
                   prefix_tokens=pre, q_sigma=q_sigma, v_mean=v_mean, perms=perms)
     return wl
+
+
+def custom_workload(lens, Hq: int, Hkv: int, d: int, bs: int, q_len: int, dtype: int, prefix_tokens: int = 0,
+                    free_frac: float = 0.1, tag: int = 99, partition_tokens: int = 512, q_sigma: float = 1.0,
+                    v_mean: float = 0.0, stride: Optional[int] = None) -> Workload:
+    """A workload with explicit context lengths (edge cases); blocks placed by a seeded shuffle."""
+    lens = np.asarray(lens, dtype=np.int32)
+    seed = 0x5EED0000 + tag
+    own = sum(-(-int(L) // bs) - prefix_tokens // bs for L in lens)
+    NB = int(math.ceil((1 + free_frac) * (prefix_tokens // bs + own))) + 1
+    st = max(-(-int(L) // bs) for L in lens) if stride is None else stride
+    perm = permutation(seed, make_stream(tag, 0, K_PERM), NB)
+    tables = _tables_from_perm(perm, lens, bs, st, prefix_tokens // bs)
+    return Workload(name=f"custom{tag}", tag=tag, seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, d=d, bs=bs, q_len=q_len,
+                    dtype=dtype, context_lens=lens, num_blocks=NB, block_tables=tables, layers=1,
+                    prefix_tokens=prefix_tokens, partition_tokens=partition_tokens, q_sigma=q_sigma, v_mean=v_mean,
+                    perms=[perm])
 
 
 def layer_tables(wl: Workload, layer: int) -> np.ndarray:

@@ -1,0 +1,105 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Cache writes are compared word for word; attention outputs element-wise within
+|gpu - oracle| <= 2e-3 + 1e-2 * |oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.device as sdev
+from paged_kv_cache_223_gb300 import pagedattn as pa
+
+pytestmark = pytest.mark.gpu
+
+import gpu_harness as H  # noqa: E402
+
+
+def test_device_generator_matches_host():
+    rows = torch.tensor([0, 7, 123456, 2 ** 33 + 5], dtype=torch.int64, device=H.DEV)
+    for dt in (synth.FP16, synth.BF16):
+        for sigma, mean in ((1.0, 0.0), (8.0, 0.0), (1.0, 1.0)):
+            t = torch.empty((4, 1024), dtype=torch.int16, device=H.DEV)
+            sdev.fill_rows(t, rows, 1024, 0x5EED0001, 99, dt, sigma, mean)
+            host = synth.fill_rows16(rows.cpu().numpy(), 4, 1024, 0x5EED0001, 99, dt, sigma, mean, use_c=False)
+            assert np.array_equal(t.cpu().numpy().view(np.uint16), host)
+
+
+def test_tiny_config_full_chain():
+    """Tiny paged decode (4 sequences, lens 17/64/100/200, Hq 8, Hkv 2, d 64, bs 16, fp16): whole pool bit-exact,
+    outputs within tolerance."""
+    wl = synth.workload(1)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, hk, hv = H.oracle_reference(wl, 0, full_pool=True)
+    assert np.array_equal(H.pool_words(kc), hk)
+    assert np.array_equal(H.pool_words(vc), hv)
+    H.assert_close(out, ref, "cfg1")
+
+
+@pytest.mark.parametrize("k,batch", [(2, 8), (3, 4), (4, 16), (5, 1)])
+def test_reduced_configs(k, batch):
+    """Each workload's recipe at a reduced batch: every output and every used block checked."""
+    wl = synth.workload(k, batch=batch, layers=1)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, hk, hv = H.oracle_reference(wl, 0)
+    H.check_pool_blocks(wl, 0, kc, vc, hk, hv, range(wl.B))
+    H.assert_close(out, ref, f"cfg{k} batch {batch}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4, 5])
+def test_full_size_sampled(k):
+    """The workloads at full size, launched as the benchmark launches them; the oracle checks a sample of
+    sequences (first, middle, last) and their blocks."""
+    wl = synth.workload(k, layers=2 if k == 3 else None)
+    layer = 1 if k == 3 else 0
+    pool, kc, vc, q, tables, lens = H.build_device(wl, layer)
+    out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    seqs = sorted({0, wl.B // 2, wl.B - 1})
+    ref, hk, hv = H.oracle_reference(wl, layer, seqs)
+    H.check_pool_blocks(wl, layer, kc, vc, hk, hv, seqs)
+    H.assert_close(out[seqs], ref, f"cfg{k} full")
+    assert torch.isfinite(out.float()).all()
+
+
+EDGE = [
+    # (lens, Hq, Hkv, d, bs, q_len, dtype, prefix, partition)
+    ([1], 8, 2, 64, 16, 1, synth.FP16, 0, 512),                 # single token
+    ([5, 6, 21], 32, 8, 128, 16, 5, synth.BF16, 0, 512),        # context == q_len, just above
+    ([16, 32, 512, 513, 1024], 16, 8, 128, 16, 1, synth.FP16, 0, 512),   # block / partition boundaries
+    ([33, 64, 95], 8, 8, 64, 32, 1, synth.BF16, 0, 32),         # MHA (G = 1), bs 32, tiny partitions
+    ([700, 1000], 32, 4, 128, 32, 4, synth.FP16, 0, 256),       # G = 8, q_len 4: 32 rows
+    ([300, 517], 24, 8, 64, 16, 3, synth.BF16, 0, 64),          # G = 3, q_len 3: 9 rows
+    ([1024 + 7, 1024 + 100], 32, 8, 128, 16, 5, synth.BF16, 1024, 512),  # shared prefix + verify
+    ([2000, 31, 4097], 64, 8, 128, 16, 1, synth.FP16, 0, 512),  # ragged lengths, G = 8
+    ([516, 1030], 16, 4, 128, 16, 5, synth.FP16, 0, 512),       # draft rows straddle a partition edge
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"edge{i}" for i in range(len(EDGE))])
+def test_edge_cases(case):
+    lens, Hq, Hkv, d, bs, ql, dt, pre, part = case
+    wl = synth.custom_workload(lens, Hq, Hkv, d, bs, ql, dt, prefix_tokens=pre, partition_tokens=part,
+                               tag=200 + EDGE.index(case))
+    pool, kc, vc, q, tables, lens_d = H.build_device(wl)
+    out = pool.decode(q, tables, lens_d, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, hk, hv = H.oracle_reference(wl, 0)
+    H.check_pool_blocks(wl, 0, kc, vc, hk, hv, range(wl.B))
+    H.assert_close(out, ref, f"edge {case}")
+
+
+@pytest.mark.parametrize("stress", ["vmean", "qx8"])
+def test_stress_variants(stress):
+    """Same shapes, harder numerics: V with mean 1 (relative tolerance governs) and q x 8 (peaked softmax)."""
+    for k, batch in ((5, 1), (2, 4)):
+        wl = synth.workload(k, batch=batch, stress=stress)
+        pool, kc, vc, q, tables, lens = H.build_device(wl)
+        out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+        ref, _, _ = H.oracle_reference(wl, 0)
+        H.assert_close(out, ref, f"cfg{k} {stress}")

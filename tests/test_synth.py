@@ -67,3 +67,14 @@ def test_workload_shapes():
     assert suf.min() >= 64 and suf.max() <= 512 and w4.q_len == 5
     w5 = synth.workload(5)
     assert w5.bs == 32 and w5.num_blocks == 16384
+
+
+def test_host_c_generator_matches_numpy_definition():
+    from paged_kv_cache_223_gb300 import _build
+    _build.build_synth_host()
+    rows = np.array([0, 5, 123456789, 2 ** 40 + 3], dtype=np.int64)
+    for dt in (synth.FP16, synth.BF16):
+        for sigma, mean in ((1.0, 0.0), (8.0, 0.0), (1.0, 1.0)):
+            a = synth.fill_rows16(rows, len(rows), 1024, 0x5EED0002, 77, dt, sigma, mean, use_c=True)
+            b = synth.fill_rows16(rows, len(rows), 1024, 0x5EED0002, 77, dt, sigma, mean, use_c=False)
+            assert np.array_equal(a, b)
