@@ -193,7 +193,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     k = WORKLOADS[args.workload]
-    wl = synth.workload(k)
+    wl = synth.workload(k, layers=args.layers, batch=args.batch)
     G = GpuWorkload(wl, dev)
     total_bytes, decode_bytes = step_bytes(wl)
     kv_tokens = int(wl.context_lens.sum()) * wl.layers
@@ -233,7 +233,7 @@ def run_gpu(args):
     value = ws * total_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
 
     # end to end through the public API: pinned host inputs -> device, kernels, result -> host
-    e2e = run_e2e(G, wl, dev, max(3, args.steps // 5), barrier)
+    e2e = None if args.no_e2e else run_e2e(G, wl, dev, max(3, args.steps // 5), barrier)
 
     if rank == 0:
         peak, peak_kind = peaks()
@@ -404,6 +404,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="layer pools (workload 3 only; default 80)")
+    ap.add_argument("--batch", type=int, default=None, help="sequences (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3

@@ -246,12 +246,30 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                 }
             }
 
-        // P^T as the B operand (16 keys x 8 columns): transpose the two 8x8 halves of S^T
-        uint32_t pb[NT][2];
+        // P^T as the B operand (16 keys x 8 columns): transpose the two 8x8 halves of S^T.
+        // The MMA takes P in V's 16-bit type. bf16 keeps 8 mantissa bits, too few for short
+        // contexts whose weighted values cancel, so for bf16 P is carried as hi + lo bf16 parts
+        // (hi = bf16(P), lo = bf16(P - hi)) and P.V is two MMAs; fp16's 11 bits suffice alone.
+        constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
+        uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            pb[nt][0] = movmatrix_trans(pack2<T>(sacc[nt][0], sacc[nt][1]));
-            pb[nt][1] = movmatrix_trans(pack2<T>(sacc[nt][2], sacc[nt][3]));
+            if constexpr (SPLIT_P) {
+                float hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    hi[e] = __bfloat162float(__float2bfloat16_rn(sacc[nt][e]));
+                    lo[e] = sacc[nt][e] - hi[e];
+                }
+                pb[nt][0] = movmatrix_trans(pack2<T>(hi[0], hi[1]));
+                pb[nt][1] = movmatrix_trans(pack2<T>(hi[2], hi[3]));
+                pl[nt][0] = movmatrix_trans(pack2<T>(lo[0], lo[1]));
+                pl[nt][1] = movmatrix_trans(pack2<T>(lo[2], lo[3]));
+            } else {
+                pb[nt][0] = movmatrix_trans(pack2<T>(sacc[nt][0], sacc[nt][1]));
+                pb[nt][1] = movmatrix_trans(pack2<T>(sacc[nt][2], sacc[nt][3]));
+                pl[nt][0] = pl[nt][1] = 0u;
+            }
         }
 
         // O^T += V^T . P^T
@@ -264,7 +282,10 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_trans(addr, a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_16816<T>(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816<T>(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                    if constexpr (SPLIT_P) mma_16816<T>(o[md][nt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+                }
             }
         }
         __syncwarp();
