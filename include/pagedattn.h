@@ -148,6 +148,44 @@ pa_status pa_pool_check(pa_pool *pool, void *stream);
 int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int32_t num_seqs,
                            int32_t num_q_heads, int32_t q_len);
 
+/*
+ * Allocation-free decode.
+ *
+ * Some callers cannot allocate device memory: a plugin inside a host runtime
+ * that owns every device allocation through its own allocator and memory
+ * budget, or a latency-critical loop that must not make cudaMalloc's
+ * synchronising call. Such a caller cannot create a pool, because
+ * pa_pool_create allocates the split workspace. This entry point takes the
+ * pool geometry directly and keeps the split workspace in one static device
+ * array of PA_NOALLOC_SCRATCH_BYTES, which every GPU that runs it holds from
+ * its first call until the process exits. The pages have no counterpart to
+ * this entry point; it computes what pa_decode computes, with the same kernels.
+ *
+ *  - Inputs and outputs are the caller's, with pa_decode's layouts and meaning;
+ *    num_blocks .. dtype and partition_tokens (0 = 512) are as in pa_pool_config.
+ *  - Scratch needed when P = ceil(block_table_stride * block_size /
+ *    partition_tokens) > 1: num_seqs * q_len * num_q_heads * P * head_dim * 4
+ *    bytes (rounded up to 256) plus num_seqs * q_len * num_q_heads * P * 8.
+ *    A larger request returns PA_ERR_INVALID_ARG before anything is launched.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on a device, made with that device current, looks up the
+ *    array's device address once; make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array and leaves its contents behind. Each call
+ *    writes every scratch slot before reading it, so nothing needs clearing,
+ *    but calls that overlap on the GPU (e.g. on two streams) race on the array
+ *    and must be ordered by the caller.
+ *  - There is no status word: an out-of-range block id or context length is
+ *    clamped (the kernel does not fault) but not reported.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+pa_status pa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                            int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                            const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                            int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale,
+                            int32_t partition_tokens, void *out, void *stream);
+
 /* A static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);
 

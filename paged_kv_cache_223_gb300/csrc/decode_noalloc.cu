@@ -1,0 +1,138 @@
+// decode_noalloc.cu -- pa_decode_noalloc: the paged decode for callers that cannot allocate
+// device memory (see include/pagedattn.h). Its only scratch is the file-scope array below.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pa_internal.h"
+
+using namespace pa;
+
+namespace {
+
+constexpr size_t SCRATCH_BYTES = PA_NOALLOC_SCRATCH_BYTES;
+
+// The split pass's workspace: partition outputs followed by the (max, sum) pairs.
+// Every call writes each slot it later reads, so nothing needs clearing between calls.
+static __device__ __align__(256) unsigned char g_scratch[SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_mu;
+void *g_scratch_ptr[MAX_DEVICES] = {};
+
+// Device address of g_scratch on the current device (looked up once per device). In host
+// code the name g_scratch is only a host-side stand-in, so it is never passed to a kernel.
+cudaError_t scratch_address(int device, void **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[device] = p;
+    }
+    *out = g_scratch_ptr[device];
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode(const void *cache, int num_blocks, int Hkv, int bs, int D, int dtype, CUtensorMap *m) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * bs};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)TILE_TOKENS};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                                       const int32_t *block_tables, int32_t block_table_stride,
+                                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t q_len, float scale, int32_t partition_tokens, void *out,
+                                       void *stream) {
+    // ---- host-side validation (nothing launched on error)
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || num_kv_heads <= 0 || block_table_stride < 1 || num_seqs < 1 || q_len < 1 || q_len > 8 ||
+        num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (partition_tokens == 0) partition_tokens = 512;
+    if (partition_tokens < 0 || partition_tokens % block_size != 0 || partition_tokens > 16384)
+        return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / num_kv_heads;
+    if (G * q_len > MAX_ROWS) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const int64_t max_ctx = (int64_t)block_table_stride * block_size;
+    if (max_ctx >= ((int64_t)1 << 31)) return PA_ERR_INVALID_ARG;
+    const int64_t max_parts = (max_ctx + partition_tokens - 1) / partition_tokens;
+    if ((int64_t)num_seqs * num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    // scratch needed: per (output row, partition) head_dim floats plus one (max, sum) pair
+    const int64_t slots = (int64_t)num_seqs * q_len * num_q_heads * max_parts;
+    const int64_t o_bytes = ((slots * head_dim * 4 + 255) / 256) * 256;
+    const int64_t need = max_parts > 1 ? o_bytes + slots * 8 : 0;
+    if (need > (int64_t)SCRATCH_BYTES) return PA_ERR_INVALID_ARG;   // beyond PA_NOALLOC_SCRATCH_BYTES
+
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= MAX_DEVICES) return PA_ERR_CUDA;
+    void *scratch = nullptr;
+    if (scratch_address(device, &scratch) != cudaSuccess) return PA_ERR_CUDA;
+    CUtensorMap tmk, tmv;
+    if (!encode(k_cache, num_blocks, num_kv_heads, block_size, head_dim, dtype, &tmk) ||
+        !encode(v_cache, num_blocks, num_kv_heads, block_size, head_dim, dtype, &tmv))
+        return PA_ERR_CUDA;
+
+    DecodeParams p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.part_o = static_cast<float *>(scratch);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<unsigned char *>(scratch) + o_bytes);
+    p.status = nullptr;   // no status word on this path: bad ids / lengths are still clamped, not reported
+    p.stride = block_table_stride;
+    p.num_seqs = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.G = G;
+    p.q_len = q_len;
+    p.rows = G * q_len;
+    p.bs = block_size;
+    p.num_blocks = num_blocks;
+    p.part_tokens = partition_tokens;
+    p.max_parts = (int)max_parts;
+    p.max_ctx = (int)max_ctx;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_ns = 2000000000ull;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_decode(p, dtype, head_dim, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (max_parts > 1 && launch_merge(p, dtype, head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}

@@ -178,3 +178,29 @@ def pool_create_status(**cfg) -> int:
     if st == PA_OK:
         lib().pa_destroy(h)
     return st
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES
+_noalloc_ready = False
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, scale: float, out: torch.Tensor, partition_tokens: int = 0,
+                   stream: Optional[torch.cuda.Stream] = None) -> int:
+    """pa_decode_noalloc: the paged decode for callers that cannot allocate device memory.
+
+    The caches carry the pool geometry ([num_blocks, Hkv, block_size, d]); the split workspace is the
+    library's static device array, so nothing is allocated. Returns the pa_status code."""
+    global _noalloc_ready
+    L = lib()
+    if not _noalloc_ready:
+        P, I32 = C.c_void_p, C.c_int32
+        L.pa_decode_noalloc.argtypes = [P, P, P, I32, I32, I32, I32, I32, P, I32, P, I32, I32, I32, C.c_float, I32,
+                                        P, P]
+        L.pa_decode_noalloc.restype = C.c_int
+        _noalloc_ready = True
+    NB, Hkv, bs, d = k_cache.shape
+    B, q_len, Hq, _ = q.shape
+    return L.pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, d, _PA_DTYPE[q.dtype],
+                               _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, q_len,
+                               float(scale), partition_tokens, _ptr(out), _stream(stream))
