@@ -176,6 +176,22 @@ class GpuWorkload:
         return len(self.layers) * (1 + self.decode_launches)
 
 
+def reduce_max(value: float, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_rank_step: int, steps: int, elapsed_ms: float, world_size: int) -> float:
+    """Whole-job GB/s: the bytes all ranks processed over the slowest rank's time."""
+    return world_size * bytes_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 def step_bytes(wl: synth.Workload):
     """Algorithmic bytes of one step: per layer, the decode's (q + unique valid K/V + used table entries + lens + out)
     and the cache write's (new k/v read + slot map + the rows written)."""
@@ -225,12 +241,9 @@ def run_gpu(args):
         barrier()
     elapsed_ms = start.elapsed_time(stop)
     dec_ms = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps) for i in range(nl)]
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(elapsed_ms, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = ws * total_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = job_value(total_bytes, args.steps, elapsed_ms, ws)
 
     # end to end through the public API: pinned host inputs -> device, kernels, result -> host
     e2e = None if args.no_e2e else run_e2e(G, wl, dev, max(3, args.steps // 5), barrier)

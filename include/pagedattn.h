@@ -144,6 +144,16 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
  */
 pa_status pa_pool_check(pa_pool *pool, void *stream);
 
+/*
+ * Self-test of failure detection. Every wait of the kernels' copy pipelines is
+ * bounded: after a time limit the kernel records PA_ERR_TIMEOUT in the pool's
+ * status word and returns instead of spinning. This launches one warp that
+ * waits, through the same bounded wait, on a barrier that nothing completes;
+ * after limit_ns (at most 10 s) it records the timeout and returns, leaving
+ * the context usable. pa_pool_check then returns PA_ERR_TIMEOUT.
+ */
+pa_status pa_pool_selftest_wait(pa_pool *pool, uint64_t limit_ns, void *stream);
+
 /* Number of kernels pa_decode launches for these arguments (1, or 2 with the merge); -1 on bad args. */
 int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int32_t num_seqs,
                            int32_t num_q_heads, int32_t q_len);

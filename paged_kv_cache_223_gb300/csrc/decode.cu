@@ -375,71 +375,100 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
     }
 }
 
-// Log-sum-exp merge of the partitions of one output row (b, qi, h):
-//   M = max_p m_p,  out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p
-// Warp w folds partitions w, w+4, ... in order; the four results are folded in warp order,
-// so the result does not depend on timing.
+// Log-sum-exp merge of the partitions of one sequence's query position qi and KV head g
+// (its G output rows):
+//   M = max_p m_p,  w_p = 2^(m_p - M) (0 for an empty partition),
+//   out = sum_p w_p O_p / sum_p w_p l_p
+// Phase 1: warp r of the CTA reads all (m_p, l_p) of row r at once and leaves the weights in
+// shared memory. Phase 2: MERGE_THREADS threads are split into groups; each thread owns one
+// (row, 4 dims) pair and sums a fixed subset of partitions with independent loads; the group
+// sums are added in group order. The result does not depend on timing.
+constexpr int MERGE_THREADS = 512;
+
+// Shared-memory layout of merge_kernel, in floats: weights [G][max_parts], den [G], then the
+// float4 group sums. Each region starts on a 16-byte boundary.
+__host__ __device__ inline int merge_wt_floats(int G, int max_parts) { return (G * max_parts + 3) & ~3; }
+__host__ __device__ inline int merge_den_floats(int G) { return (G + 3) & ~3; }
+__host__ __device__ inline int merge_groups(int pairs) { return MERGE_THREADS / pairs > 0 ? MERGE_THREADS / pairs : 1; }
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
-    constexpr int VPL = D / 32;   // values per lane
-    __shared__ float s_o[4][D];
-    __shared__ float s_ml[4][2];
-    const int row = blockIdx.x;
-    const int b = row / (p.q_len * p.Hq);
+__global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams p) {
+    extern __shared__ float msm[];                 // weights [G][max_parts], den [G], sums [groups][G*D]
+    const int unit = blockIdx.x;                   // (b, qi, g)
+    const int g = unit % p.Hkv;
+    const int bq = unit / p.Hkv;                   // b * q_len + qi
+    const int b = bq / p.q_len;
     int L = __ldg(p.context_lens + b);
     L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
     const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
     if (nparts <= 1) return;
+    const int G = p.G;
+    float *wt = msm;                               // [G][max_parts]
+    float *den = wt + merge_wt_floats(G, p.max_parts);   // [G]
+    float4 *sums = reinterpret_cast<float4 *>(den + merge_den_floats(G));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float M = -INFINITY, ls = 0.f, acc[VPL];
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
-    const float2 *ml = p.part_ml + (int64_t)row * p.max_parts;
-    const float *po = p.part_o + (int64_t)row * p.max_parts * D;
-    for (int pp = warp; pp < nparts; pp += 4) {
-        const float2 v = ml[pp];
-        if (!(v.y > 0.f)) continue;
-        const float Mn = fmaxf(M, v.x);
-        const float a = exp2f(M - Mn);
-        const float c = exp2f(v.x - Mn);
-        ls = ls * a + v.y * c;
-        const float *src = po + (int64_t)pp * D + lane * VPL;
-        if (VPL == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(src);
-            acc[0] = acc[0] * a + c * x.x;
-            acc[1] = acc[1] * a + c * x.y;
-            acc[2] = acc[2] * a + c * x.z;
-            acc[3] = acc[3] * a + c * x.w;
-        } else {
-#pragma unroll
-            for (int k = 0; k < VPL; ++k) acc[k] = acc[k] * a + c * src[k];
+    const int64_t row0 = (int64_t)bq * p.Hq + g * G;   // first output row of the unit
+
+    for (int r = warp; r < G; r += MERGE_THREADS / 32) {
+        const float2 *ml = p.part_ml + (row0 + r) * p.max_parts;
+        float M = -INFINITY;
+        for (int pp = lane; pp < nparts; pp += 32) {
+            const float2 v = __ldcg(ml + pp);
+            if (v.y > 0.f) M = fmaxf(M, v.x);
         }
-        M = Mn;
-    }
 #pragma unroll
-    for (int k = 0; k < VPL; ++k) s_o[warp][lane * VPL + k] = acc[k];
-    if (lane == 0) {
-        s_ml[warp][0] = M;
-        s_ml[warp][1] = ls;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float ds = 0.f;
+        for (int pp = lane; pp < nparts; pp += 32) {
+            const float2 v = __ldcg(ml + pp);
+            const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+            wt[r * p.max_parts + pp] = w;
+            ds += w * v.y;
+        }
+        // fixed-order sum over lanes
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
+        if (lane == 0) den[r] = ds;
     }
     __syncthreads();
-    for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
-        float Mt = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) Mt = fmaxf(Mt, s_ml[w][0]);
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float sc = s_ml[w][0] == -INFINITY ? 0.f : exp2f(s_ml[w][0] - Mt);
-            num += sc * s_o[w][dim];
-            den += sc * s_ml[w][1];
+
+    const int pairs = G * (D / 4);
+    const int groups = merge_groups(pairs);
+    for (int t = threadIdx.x; t < pairs * groups; t += MERGE_THREADS) {
+        const int pair = t % pairs;
+        const int grp = t / pairs;
+        const int r = pair / (D / 4);
+        const int d4 = pair - r * (D / 4);
+        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + (row0 + r) * p.max_parts * D) + d4;
+        const float *w = wt + r * p.max_parts;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int pp = grp; pp < nparts; pp += groups) {
+            const float c = w[pp];
+            const float4 x = __ldcg(po + (int64_t)pp * (D / 4));
+            acc.x += c * x.x;
+            acc.y += c * x.y;
+            acc.z += c * x.z;
+            acc.w += c * x.w;
         }
-        const float r = num / den;
-        T *out = reinterpret_cast<T *>(p.out) + (int64_t)row * D + dim;
-        if constexpr (std::is_same<T, __half>::value)
-            *out = __float2half_rn(r);
-        else
-            *out = __float2bfloat16_rn(r);
+        sums[grp * pairs + pair] = acc;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < pairs; q += MERGE_THREADS) {
+        float4 t = sums[q];
+        for (int k = 1; k < groups; ++k) {
+            const float4 u = sums[k * pairs + q];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
+        }
+        const int r = q / (D / 4);
+        const int d4 = q - r * (D / 4);
+        const float inv = 1.f / den[r];
+        T *out = reinterpret_cast<T *>(p.out) + (row0 + r) * D + d4 * 4;
+        const uint32_t lo = pack2<T>(t.x * inv, t.y * inv), hi = pack2<T>(t.z * inv, t.w * inv);
+        *reinterpret_cast<uint2 *>(out) = make_uint2(lo, hi);
     }
 }
 
@@ -481,15 +510,26 @@ cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const 
     return cudaErrorInvalidValue;
 }
 
+size_t merge_smem_bytes(int G, int max_parts, int head_dim) {
+    const int pairs = G * (head_dim / 4);
+    return (size_t)(merge_wt_floats(G, max_parts) + merge_den_floats(G)) * sizeof(float) +
+           (size_t)merge_groups(pairs) * pairs * sizeof(float4);
+}
+
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
-    const int64_t rows = (int64_t)p.num_seqs * p.q_len * p.Hq;
+    const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv;
+    const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim);
+    cudaError_t e = cudaSuccess;
+#define PA_MERGE(TT, DD)                                                                                       \
+    e = cudaFuncSetAttribute(merge_kernel<TT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
+    if (e != cudaSuccess) return e;                                                                            \
+    merge_kernel<TT, DD><<<(unsigned)units, MERGE_THREADS, smem, stream>>>(p);
     if (dtype == PA_FP16) {
-        if (head_dim == 128) merge_kernel<__half, 128><<<(unsigned)rows, 128, 0, stream>>>(p);
-        else merge_kernel<__half, 64><<<(unsigned)rows, 128, 0, stream>>>(p);
+        if (head_dim == 128) { PA_MERGE(__half, 128) } else { PA_MERGE(__half, 64) }
     } else {
-        if (head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<(unsigned)rows, 128, 0, stream>>>(p);
-        else merge_kernel<__nv_bfloat16, 64><<<(unsigned)rows, 128, 0, stream>>>(p);
+        if (head_dim == 128) { PA_MERGE(__nv_bfloat16, 128) } else { PA_MERGE(__nv_bfloat16, 64) }
     }
+#undef PA_MERGE
     return cudaGetLastError();
 }
 

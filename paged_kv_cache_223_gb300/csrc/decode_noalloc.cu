@@ -94,6 +94,7 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
     if (max_ctx >= ((int64_t)1 << 31)) return PA_ERR_INVALID_ARG;
     const int64_t max_parts = (max_ctx + partition_tokens - 1) / partition_tokens;
     if ((int64_t)num_seqs * num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    if (max_parts > 1 && merge_smem_bytes(G, (int)max_parts, head_dim) > MAX_SMEM_PER_CTA) return PA_ERR_UNSUPPORTED;
     // scratch needed: per (output row, partition) head_dim floats plus one (max, sum) pair
     const int64_t slots = (int64_t)num_seqs * q_len * num_q_heads * max_parts;
     const int64_t o_bytes = ((slots * head_dim * 4 + 255) / 256) * 256;

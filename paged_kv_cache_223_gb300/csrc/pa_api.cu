@@ -230,6 +230,7 @@ static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_
     const int64_t max_parts = (max_ctx + pool->part_tokens - 1) / pool->part_tokens;
     if (max_parts > 1 && (int64_t)num_seqs * q_len * num_q_heads * max_parts > pool->ws_slots) return PA_ERR_INVALID_ARG;
     if ((int64_t)num_seqs * c.num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    if (max_parts > 1 && merge_smem_bytes(G, (int)max_parts, c.head_dim) > MAX_SMEM_PER_CTA) return PA_ERR_UNSUPPORTED;
     p.stride = stride;
     p.num_seqs = num_seqs;
     p.Hq = num_q_heads;
@@ -286,6 +287,14 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
+}
+
+pa_status pa_pool_selftest_wait(pa_pool *pool, uint64_t limit_ns, void *stream) {
+    if (!pool || limit_ns > 10ull * 1000000000ull) return PA_ERR_INVALID_ARG;
+    DeviceGuard g(pool->cfg.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    return launch_wait_selftest(pool->status, limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                                          : PA_ERR_CUDA;
 }
 
 pa_status pa_pool_check(pa_pool *pool, void *stream) {

@@ -60,6 +60,9 @@ cudaError_t launch_cache_write(const CacheWriteParams &p, int sm_count, cudaStre
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
                           const CUtensorMap &tmv, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int nt);
+size_t merge_smem_bytes(int G, int max_parts, int head_dim);
+constexpr size_t MAX_SMEM_PER_CTA = 227 * 1024;
 
 }  // namespace pa

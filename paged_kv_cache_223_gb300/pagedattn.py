@@ -57,6 +57,8 @@ def lib() -> C.CDLL:
             L.pa_cache_write.argtypes = [P, P, P, P, I32, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
             L.pa_pool_check.argtypes = [P, P]
+            L.pa_pool_selftest_wait.argtypes = [P, C.c_uint64, P]
+            L.pa_pool_selftest_wait.restype = C.c_int
             L.pa_decode_launches.argtypes = [P, I32, I32, I32, I32]
             L.pa_decode_launches.restype = I32
             L.pa_status_string.argtypes = [C.c_int]
@@ -164,6 +166,10 @@ class Pool:
 
     def launches(self, block_table_stride: int, num_seqs: int, num_q_heads: int, q_len: int) -> int:
         return lib().pa_decode_launches(self.handle, block_table_stride, num_seqs, num_q_heads, q_len)
+
+    def selftest_wait(self, limit_ns: int, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Run the bounded-wait self-test kernel (a wait that nothing completes; see pa_pool_selftest_wait)."""
+        _check(lib().pa_pool_selftest_wait(self.handle, limit_ns, _stream(stream)), "pa_pool_selftest_wait")
 
     def check(self, stream: Optional[torch.cuda.Stream] = None) -> int:
         """Synchronise and return (and clear) the device status: PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_TIMEOUT."""

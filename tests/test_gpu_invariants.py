@@ -124,3 +124,17 @@ def test_host_side_argument_errors():
     st = L.pa_decode(pool.handle, q.data_ptr(), None, None, tables.data_ptr(), tables.shape[1], lens.data_ptr(), 1,
                      16, 5, 0.125, out.data_ptr(), None)
     assert st in (pa.PA_ERR_INVALID_ARG, pa.PA_ERR_UNSUPPORTED)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait that nothing completes gives up after its limit, reports PA_ERR_TIMEOUT, and the next decode
+    on the same context still runs and is correct."""
+    wl = synth.custom_workload([300, 77], 16, 4, 128, 16, 1, synth.FP16, tag=64)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    pool.selftest_wait(2_000_000)           # 2 ms
+    assert pool.check() == pa.PA_ERR_TIMEOUT
+    assert pool.check() == pa.PA_OK
+    out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _, _ = H.oracle_reference(wl, 0)
+    H.assert_close(out, ref, "decode after a timed-out wait")

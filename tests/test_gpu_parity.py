@@ -78,6 +78,7 @@ EDGE = [
     ([1024 + 7, 1024 + 100], 32, 8, 128, 16, 5, synth.BF16, 1024, 512),  # shared prefix + verify
     ([2000, 31, 4097], 64, 8, 128, 16, 1, synth.FP16, 0, 512),  # ragged lengths, G = 8
     ([516, 1030], 16, 4, 128, 16, 5, synth.FP16, 0, 512),       # draft rows straddle a partition edge
+    ([1500, 40], 32, 1, 128, 16, 1, synth.BF16, 0, 256),        # G = 32 (one KV head): 32 rows, wide merge
 ]
 
 
