@@ -56,6 +56,7 @@ def lib():
             L.oracle_bf16_to_double.restype = C.c_double
             L.oracle_cache_write.argtypes = [P, P, P, P, P, C.c_int64, C.c_int64, C.c_int, C.c_int, C.c_int]
             L.oracle_gather.argtypes = [P, P, C.c_int64, C.c_int64, C.c_int, C.c_int, C.c_int, P]
+            L.oracle_copy_blocks.argtypes = [P, P, P, C.c_int64, C.c_int64, C.c_int, C.c_int, C.c_int]
             L.oracle_attention.argtypes = [P, P, P, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                            C.c_float, P, P]
             L.oracle_paged_attention.argtypes = [P, P, P, P, C.c_int64, P, P, C.c_int, C.c_int64, C.c_int,
@@ -64,9 +65,10 @@ def lib():
             L.oracle_attention_partitions.argtypes = [P, P, P, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int,
                                                       C.c_int, C.c_float, C.c_int64, P, P, P]
             L.oracle_lse_merge.argtypes = [C.c_int64, P, P, P, C.c_int, P]
+            L.oracle_spec_verify.argtypes = [P, P, P, P, P, C.c_int64, C.c_int, C.c_int64, P, P]
             L.oracle_num_cpus.argtypes = []
-            for f in ("oracle_cache_write", "oracle_gather", "oracle_attention", "oracle_paged_attention",
-                      "oracle_attention_partitions", "oracle_lse_merge", "oracle_num_cpus"):
+            for f in ("oracle_cache_write", "oracle_gather", "oracle_copy_blocks", "oracle_attention", "oracle_paged_attention",
+                      "oracle_attention_partitions", "oracle_lse_merge", "oracle_num_cpus", "oracle_spec_verify"):
                 getattr(L, f).restype = C.c_int
             _libs[path] = L
     return _libs[path]
@@ -109,6 +111,13 @@ def cache_write(k_pool: np.ndarray, v_pool: np.ndarray, k: np.ndarray, v: np.nda
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     _check(lib().oracle_cache_write(_p(k_pool), _p(v_pool), _p(k), _p(v), _p(sm), len(sm), NB, bs, Hkv, d),
            "cache_write")
+
+
+def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, pairs) -> None:
+    """In-place copy of block pairs (src, dst) in both pools."""
+    NB, Hkv, bs, d = k_pool.shape
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    _check(lib().oracle_copy_blocks(_p(k_pool), _p(v_pool), _p(pr), len(pr), NB, bs, Hkv, d), "copy_blocks")
 
 
 def gather(pool: np.ndarray, table_row: np.ndarray, L: int) -> np.ndarray:
@@ -177,3 +186,19 @@ def lse_merge(m: np.ndarray, l: np.ndarray, o: np.ndarray) -> np.ndarray:
 
 def num_cpus() -> int:
     return lib().oracle_num_cpus()
+
+
+def spec_verify(p: np.ndarray, q: np.ndarray, draft: np.ndarray, u: np.ndarray, v: np.ndarray):
+    """Speculative rejection sampling. p [B, K+1, V], q [B, K, V] fp32; draft int32 [B, K]; u fp32 [B, K];
+    v fp32 [B]. Returns (out int32 [B, K+1], n_out int32 [B])."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    draft = np.ascontiguousarray(draft, dtype=np.int32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    B, K1, V = p.shape
+    out = np.empty((B, K1), dtype=np.int32)
+    n = np.empty(B, dtype=np.int32)
+    _check(lib().oracle_spec_verify(_p(p), _p(q), _p(draft), _p(u), _p(v), B, K1 - 1, V, _p(out), _p(n)),
+           "spec_verify")
+    return out, n

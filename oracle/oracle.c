@@ -14,6 +14,8 @@
  *                boundary takes one new block from the free pool; itimpress.au
  *                "PagedAttention, ...", section 1: K and V of every previous
  *                token are kept so they are not recomputed.)
+ *  copy-on-write A shared block about to be written is first copied whole to a
+ *                fresh block (yangyu.win blog #54, section 5 question 2).
  *  gather        Logical token t of a sequence lives in physical block
  *                block_table[t / block_size] at offset t % block_size.
  *                (yangyu.win blog #54, section 2.2 figure: tokens 0-15 -> page 7,
@@ -27,6 +29,14 @@
  *                With q_len > 1 (verifying draft tokens in one pass:
  *                itimpress.au section 1, yangyu.win section 2.4) query row qi sits
  *                at position L - q_len + qi and sees tokens 0 .. L - q_len + qi.
+ *  verify-accept Speculative rejection sampling over the target's verify pass
+ *                (yangyu.win blog #54, section 5 question 3; maths.nthquan ch. 17
+ *                "Speculative decoding", algorithm steps 3-4): draft token x_i is
+ *                kept with probability min(1, p_i(x_i) / q_i(x_i)); the first
+ *                rejected position is resampled from max(0, p_i - q_i)
+ *                renormalised and later drafts are dropped; if every draft is
+ *                kept, one more token is drawn from the target's next
+ *                distribution. The uniform draws are inputs.
  *  partitions    The context is cut into fixed partitions; each yields its own
  *                (max, sum of exponentials, unnormalised weighted V), and a
  *                reduction combines them (maths.nthquan ch. 17 "Scaling and
@@ -102,6 +112,24 @@ int oracle_cache_write(uint16_t *k_pool, uint16_t *v_pool, const uint16_t *k, co
             memcpy(k_pool + dst, k + src, (size_t)d * sizeof(uint16_t));
             memcpy(v_pool + dst, v + src, (size_t)d * sizeof(uint16_t));
         }
+    }
+    return OR_OK;
+}
+
+/*
+ * Copy-on-write copy: block pairs[2i] -> block pairs[2i+1] of both pools, every KV head, raw
+ * words (yangyu.win blog #54, section 5 question 2: a diverging sequence gets its own copy of
+ * the shared block it is about to write).
+ */
+int oracle_copy_blocks(uint16_t *k_pool, uint16_t *v_pool, const int32_t *pairs, int64_t n, int64_t num_blocks,
+                       int bs, int Hkv, int d) {
+    if (!k_pool || !v_pool || (n > 0 && !pairs) || bs <= 0 || Hkv <= 0 || d <= 0) return OR_ERR_ARG;
+    const int64_t words = (int64_t)Hkv * bs * d;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return OR_ERR_BOUNDS;
+        memcpy(k_pool + dst * words, k_pool + src * words, (size_t)words * sizeof(uint16_t));
+        memcpy(v_pool + dst * words, v_pool + src * words, (size_t)words * sizeof(uint16_t));
     }
     return OR_OK;
 }
@@ -368,4 +396,89 @@ int oracle_lse_merge(int64_t np_, const double *m, const double *l, const double
     }
     for (int k = 0; k < d; ++k) out[k] /= den;
     return OR_OK;
+}
+
+/* ------------------------------------------------ speculative rejection sampling */
+
+/*
+ * Index of the first j with sum_{t <= j} w_t > v * sum_t w_t (serial fp64 sums). When the total
+ * is 0 the result is -1.
+ */
+static int64_t inverse_cdf(const double *w, int64_t V, double v) {
+    double total = 0.0;
+    for (int64_t t = 0; t < V; ++t) total += w[t];
+    if (!(total > 0.0)) return -1;
+    const double target = v * total;
+    double c = 0.0;
+    for (int64_t t = 0; t < V; ++t) {
+        c += w[t];
+        if (c > target) return t;
+    }
+    for (int64_t t = V - 1; t >= 0; --t)       /* v * total rounded up to total: the last token with mass */
+        if (w[t] > 0.0) return t;
+    return -1;
+}
+
+/*
+ * One batch of verifications.
+ *   p      fp32 [B, K+1, V]  target distributions at the K draft positions and the next one
+ *   q      fp32 [B, K, V]    draft distributions
+ *   draft  int32 [B, K]      draft tokens
+ *   u      fp32 [B, K]       uniforms in [0, 1) for the accept tests
+ *   v      fp32 [B]          uniform in [0, 1) for the one token drawn at the end
+ *   out    int32 [B, K+1]    emitted tokens (kept drafts, then the drawn token), -1 after them
+ *   n_out  int32 [B]         number of emitted tokens (kept drafts + 1)
+ * The accept test is evaluated in fp32 as u * q < p (the same comparison as
+ * u < p / q for q > 0, without a division). The drawn token is the inverse CDF
+ * of max(0, p_i - q_i) (or of p_K when all drafts are kept) at v, in fp64;
+ * when the residual has no mass, p_i itself is used.
+ */
+int oracle_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
+                       int64_t B, int K, int64_t V, int32_t *out, int32_t *n_out) {
+    if (!p || !q || !draft || !u || !v || !out || !n_out || B < 0 || K < 0 || V <= 0) return OR_ERR_ARG;
+    double *w = (double *)malloc((size_t)V * sizeof(double));
+    if (!w) return OR_ERR_OOM;
+    int rc = OR_OK;
+    for (int64_t b = 0; b < B && rc == OR_OK; ++b) {
+        int32_t *o = out + b * (K + 1);
+        for (int i = 0; i <= K; ++i) o[i] = -1;
+        int n = 0;
+        int rejected = -1;
+        for (int i = 0; i < K; ++i) {
+            const int32_t x = draft[b * K + i];
+            if (x < 0 || x >= V) { rc = OR_ERR_BOUNDS; break; }
+            const float pi = p[(b * (K + 1) + i) * V + x];
+            const float qi = q[(b * K + i) * V + x];
+            const float uq = u[b * K + i] * qi;       /* one fp32 rounding */
+            if (uq < pi) {
+                o[n++] = x;
+            } else {
+                rejected = i;
+                break;
+            }
+        }
+        if (rc != OR_OK) break;
+        int64_t tok;
+        if (rejected >= 0) {
+            const float *pr = p + (b * (K + 1) + rejected) * V;
+            const float *qr = q + (b * K + rejected) * V;
+            for (int64_t t = 0; t < V; ++t) {
+                const double r = (double)pr[t] - (double)qr[t];
+                w[t] = r > 0.0 ? r : 0.0;
+            }
+            tok = inverse_cdf(w, V, (double)v[b]);
+            if (tok < 0) {
+                for (int64_t t = 0; t < V; ++t) w[t] = pr[t] > 0.0f ? (double)pr[t] : 0.0;
+                tok = inverse_cdf(w, V, (double)v[b]);
+            }
+        } else {
+            const float *pr = p + (b * (K + 1) + K) * V;
+            for (int64_t t = 0; t < V; ++t) w[t] = pr[t] > 0.0f ? (double)pr[t] : 0.0;
+            tok = inverse_cdf(w, V, (double)v[b]);
+        }
+        o[n++] = (int32_t)tok;
+        n_out[b] = n;
+    }
+    free(w);
+    return rc;
 }

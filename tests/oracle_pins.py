@@ -353,7 +353,86 @@ def pin_cache_write_skip_and_untouched():
     assert np.array_equal(kp, expect_k) and np.array_equal(vp, expect_v)
 
 
+def pin_copy_on_write_equals_private_write():
+    """A sample that shares a prompt's blocks, copies the partly filled last block and writes its own token
+    into the copy, gathers exactly its logical tokens; the prompt's owner still gathers its own; the copy
+    touches nothing else (yangyu.win blog #54 section 5 question 2: copy-on-write on divergence)."""
+    rng = _rng(10)
+    NB, Hkv, bs, d = 8, 2, 16, 8
+    kp = np.zeros((NB, Hkv, bs, d), np.uint16)
+    vp = np.zeros_like(kp)
+    prompt_k = words(rng, (40, Hkv, d), FP16)
+    prompt_v = words(rng, (40, Hkv, d), FP16)
+    table_a = np.array([5, 1, 6], np.int32)                 # 40 tokens: blocks 5, 1 and 6 (8 tokens used)
+    t = np.arange(40)
+    oracle.cache_write(kp, vp, prompt_k, prompt_v, table_a[t // bs].astype(np.int64) * bs + t % bs)
+    before = (kp.copy(), vp.copy())
+    # sample B shares blocks 5, 1, 6; its token 40 goes into block 6 -> copy 6 to the free block 3 first
+    table_b = np.array([5, 1, 3], np.int32)
+    oracle.copy_blocks(kp, vp, [(6, 3)])
+    new_k = words(rng, (1, Hkv, d), FP16)
+    new_v = words(rng, (1, Hkv, d), FP16)
+    oracle.cache_write(kp, vp, new_k, new_v, np.array([3 * bs + 40 % bs]))
+    assert np.array_equal(oracle.gather(kp, table_b, 41), np.concatenate([prompt_k, new_k]))
+    assert np.array_equal(oracle.gather(vp, table_b, 41), np.concatenate([prompt_v, new_v]))
+    assert np.array_equal(oracle.gather(kp, table_a, 40), prompt_k)
+    changed = np.argwhere((kp != before[0]).any(axis=(1, 2, 3))).ravel().tolist()
+    assert changed == [3]
+
+
+def _normalised(rng, shape):
+    x = rng.random(shape).astype(np.float64) ** 3
+    return (x / x.sum(-1, keepdims=True)).astype(np.float32)
+
+
+def pin_spec_verify_is_lossless():
+    """The first emitted token is distributed as the target p, whatever the draft q (yangyu.win blog #54,
+    section 5 question 3: P(x) = min(q(x), p(x)) + max(0, p(x) - q(x)) = p(x)). Checked by quadrature over the
+    draft token x ~ q and midpoint grids of the two uniforms."""
+    rng = _rng(11)
+    V, N = 6, 120
+    for trial in range(3):
+        p = _normalised(rng, (V,))
+        q = _normalised(rng, (V,))
+        grid = (np.arange(N) + 0.5) / N
+        xs, us, vs = np.meshgrid(np.arange(V), grid, grid, indexing="ij")
+        B = xs.size
+        P = np.broadcast_to(np.stack([p, _normalised(rng, (V,))]), (B, 2, V))
+        Q = np.broadcast_to(q, (B, 1, V))
+        out, n = oracle.spec_verify(P, Q, xs.reshape(B, 1), us.reshape(B, 1).astype(np.float32),
+                                    vs.reshape(B).astype(np.float32))
+        w = q[xs.reshape(B)] / (N * N)
+        freq = np.bincount(out[:, 0], weights=w, minlength=V)
+        assert np.allclose(freq, p, atol=0.02), (trial, freq, p)
+        assert ((n == 1) | (n == 2)).all()
+
+
+def pin_spec_verify_special_cases():
+    rng = _rng(12)
+    V, K, B = 50, 4, 64
+    p = _normalised(rng, (B, K + 1, V))
+    draft = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K)).astype(np.float32)
+    v = rng.random(B).astype(np.float32)
+    # draft == target: every draft kept, then one token from p_K at v (inverse CDF == numpy searchsorted)
+    out, n = oracle.spec_verify(p, p[:, :K], draft, u, v)
+    assert (n == K + 1).all() and np.array_equal(out[:, :K], draft)
+    for b in range(B):
+        c = np.cumsum(p[b, K].astype(np.float64))
+        assert out[b, K] == np.searchsorted(c, float(v[b]) * c[-1], side="right")
+    # the target gives the drafted token no mass: rejected at once, never resampled to it
+    p0 = p.copy()
+    p0[np.arange(B), 0, draft[:, 0]] = 0.0
+    q = _normalised(rng, (B, K, V))
+    out, n = oracle.spec_verify(p0, q, draft, u, v)
+    assert (n == 1).all() and (out[:, 0] != draft[:, 0]).all() and (out[:, 1:] == -1).all()
+    # the resampled token comes from max(0, p - q): its residual mass is positive
+    r = np.maximum(0.0, p0[np.arange(B), 0].astype(np.float64) - q[:, 0].astype(np.float64))
+    assert (r[np.arange(B), out[:, 0]] > 0).all()
+
+
 ALL_PINS = [pin_decode_fp16, pin_decode_bf16, pin_mapping_yangyu, pin_mapping_tanhdev, pin_kv_size_closed_form,
             pin_sdpa_contiguous, pin_paged_equals_contiguous_under_permutation, pin_closed_forms, pin_weights,
             pin_gqa_is_mha_with_duplicated_heads, pin_verify_rows_are_decodes, pin_shared_prefix_equals_duplicated,
-            pin_split_merge_equals_unsplit, pin_cache_write_skip_and_untouched]
+            pin_split_merge_equals_unsplit, pin_cache_write_skip_and_untouched, pin_copy_on_write_equals_private_write,
+            pin_spec_verify_is_lossless, pin_spec_verify_special_cases]

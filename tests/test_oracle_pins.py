@@ -42,6 +42,13 @@ MUTANTS = {
     "merge_weight_sign": ("double w = exp(m[p] - M);", "double w = exp(M - m[p]);"),
     "partition_no_shift": ("double e = exp(s[t - t0] - mx);", "double e = exp(s[t - t0]);"),
     "partition_tail": ("if (t1 > last + 1) t1 = last + 1;", "if (t1 > last + 2) t1 = last + 2;"),
+    "copy_wrong_direction": ("memcpy(k_pool + dst * words, k_pool + src * words", "memcpy(k_pool + src * words, k_pool + dst * words"),
+    "copy_one_head": ("const int64_t words = (int64_t)Hkv * bs * d;", "const int64_t words = (int64_t)bs * d;"),
+    "spec_resample_from_p": ("const double r = (double)pr[t] - (double)qr[t];", "const double r = (double)pr[t];"),
+    "spec_resample_q_minus_p": ("const double r = (double)pr[t] - (double)qr[t];", "const double r = (double)qr[t] - (double)pr[t];"),
+    "spec_accept_inverted": ("if (uq < pi) {", "if (uq > pi) {"),
+    "spec_bonus_wrong_row": ("const float *pr = p + (b * (K + 1) + K) * V;", "const float *pr = p + (b * (K + 1) + K - 1) * V;"),
+    "spec_cdf_off_by_one": ("if (c > target) return t;", "if (c > target) return t > 0 ? t - 1 : 0;"),
     "weights_unmasked": ("w[t] = t <= last ? s[t] / l : 0.0;", "w[t] = t <= last ? s[t] / l : 1e-300;"),
 }
 
