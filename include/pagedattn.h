@@ -145,6 +145,87 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
 pa_status pa_pool_check(pa_pool *pool, void *stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Block manager (host side) and copy-on-write.
+ *
+ * The pool's physical blocks are handed out from one shared free pool; a
+ * block named by several block tables (a shared prompt, parallel samples)
+ * carries a reference count; before a sequence writes into a block it shares,
+ * the block is copied to a private one (copy-on-write). (yangyu.win blog #54,
+ * section 5 question 2; itimpress.au section 1.) The allocator is plain host
+ * memory and host code, thread-safe, and never touches the GPU; the copy is
+ * pa_copy_blocks. A failed call changes nothing.
+ */
+typedef struct pa_block_allocator pa_block_allocator;
+
+/* An allocator of num_blocks blocks of block_size tokens, all free. */
+pa_status pa_allocator_create(int32_t num_blocks, int32_t block_size, pa_block_allocator **out);
+void pa_allocator_destroy(pa_block_allocator *allocator);
+
+/* Free blocks left; the reference count of one block (0 = free). -1 on a bad argument. */
+int32_t pa_allocator_num_free(pa_block_allocator *allocator);
+int32_t pa_allocator_ref_count(pa_block_allocator *allocator, int32_t block_id);
+
+/* Take n free blocks (reference count 1 each) into ids[n]; PA_ERR_OOM if fewer are free. */
+pa_status pa_allocator_alloc(pa_block_allocator *allocator, int32_t n, int32_t *ids);
+
+/* One more reference to each listed live block (a new table shares them). */
+pa_status pa_allocator_fork(pa_block_allocator *allocator, const int32_t *ids, int32_t n);
+
+/* Drop one reference per listed id (an id may repeat); blocks reaching 0 return to the free pool. */
+pa_status pa_allocator_free(pa_block_allocator *allocator, const int32_t *ids, int32_t n);
+
+/*
+ * Copy-on-write before writing into block_id: if it is shared (count > 1), one
+ * reference is dropped, a free block is taken into *out_id and *copy = 1 (the
+ * caller copies block_id -> *out_id with pa_copy_blocks before writing);
+ * otherwise *out_id = block_id and *copy = 0.
+ */
+pa_status pa_allocator_cow(pa_block_allocator *allocator, int32_t block_id, int32_t *out_id, int32_t *copy);
+
+/*
+ * Append n_new tokens to a sequence of *len tokens whose block-table row
+ * (host int32 [stride]) holds ceil(*len / block_size) live blocks: takes a new
+ * block each time a token crosses a block boundary, copy-on-writes the partly
+ * filled last block if it is shared (then copy_pair = {old, new} and
+ * *n_copies = 1, else 0), writes each new token's slot
+ * (block * block_size + offset) to slots[n_new] (host int64), and advances *len.
+ */
+pa_status pa_allocator_append(pa_block_allocator *allocator, int32_t *table_row, int32_t stride, int32_t *len,
+                              int32_t n_new, int64_t *slots, int32_t *copy_pair, int32_t *n_copies);
+
+/*
+ * Copy whole blocks on the device: for i < n, block pairs[2i] -> block
+ * pairs[2i+1] of both caches (every KV head), raw words. pairs is a device
+ * int32 [n][2]; destinations must be distinct and not sources of another pair.
+ * Ids outside the pool are skipped and flagged (PA_ERR_DEVICE_BOUNDS).
+ * k_cache/v_cache NULL = the pool's own.
+ */
+pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k_cache, void *v_cache, void *stream);
+
+/*
+ * Speculative rejection sampling after the target model verified num_draft
+ * draft tokens in one pass (yangyu.win blog #54, section 5 question 3;
+ * maths.nthquan ch. 17 "Speculative decoding"). For each sequence b, draft
+ * x_i is kept while u_i * q_i(x_i) < p_i(x_i) (fp32; i.e. with probability
+ * min(1, p/q)); the first rejected position is resampled from
+ * max(0, p_i - q_i) renormalised (from p_i if that has no mass) and later
+ * drafts are dropped; if all are kept, one more token is drawn from
+ * p_num_draft. Draws use the inverse CDF at v_b, summed in fp64.
+ *   p      device fp32 [num_seqs, num_draft + 1, vocab]  target distributions
+ *   q      device fp32 [num_seqs, num_draft, vocab]      draft distributions
+ *   draft  device int32 [num_seqs, num_draft]            a token outside the vocabulary counts as rejected
+ *   u      device fp32 [num_seqs, num_draft]  uniforms in [0, 1) for the accept tests
+ *   v      device fp32 [num_seqs]              uniforms in [0, 1) for the final draw
+ *   out    device int32 [num_seqs, num_draft + 1]  kept drafts, then the drawn token, then -1
+ *   n_out  device int32 [num_seqs]             tokens emitted (kept drafts + 1)
+ * num_draft <= 64. No pool is needed.
+ */
+pa_status pa_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
+                         int32_t num_seqs, int32_t num_draft, int64_t vocab, int32_t *out, int32_t *n_out,
+                         void *stream);
+
+/*
  * Self-test of failure detection. Every wait of the kernels' copy pipelines is
  * bounded: after a time limit the kernel records PA_ERR_TIMEOUT in the pool's
  * status word and returns instead of spinning. This launches one warp that

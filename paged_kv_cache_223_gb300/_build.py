@@ -64,7 +64,7 @@ def _build_so(name: str, srcs: List[str], deps: List[str], out: str, includes: L
 
 def build_cuda(force: bool = False) -> str:
     csrc = os.path.join(PKG, "csrc")
-    srcs = sorted(glob.glob(os.path.join(csrc, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cpp")))
     deps = sorted(glob.glob(os.path.join(csrc, "*.h")) + glob.glob(os.path.join(csrc, "*.cuh")) +
                   [os.path.join(INCLUDE, "pagedattn.h")])
     return _build_so("pagedattn", srcs, deps, LIB, [INCLUDE, csrc], force)

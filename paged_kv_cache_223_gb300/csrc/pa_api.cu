@@ -289,6 +289,43 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     return PA_OK;
 }
 
+pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k_cache, void *v_cache,
+                         void *stream) {
+    if (!pool || n < 0) return PA_ERR_INVALID_ARG;
+    if (n == 0) return PA_OK;
+    if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 3u)) return PA_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    if (!k_cache) {
+        k_cache = pool->k_cache;
+        v_cache = pool->v_cache;
+    }
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    const pa_pool_config &c = pool->cfg;
+    DeviceGuard g(c.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    const int64_t vec_per_block = (int64_t)c.num_kv_heads * c.block_size * c.head_dim / 8;
+    return launch_copy_blocks(pairs, n, k_cache, v_cache, vec_per_block, c.num_blocks, pool->status, pool->sm_count,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
+                         int32_t num_seqs, int32_t num_draft, int64_t vocab, int32_t *out, int32_t *n_out,
+                         void *stream) {
+    if (num_seqs < 0 || num_draft < 0 || num_draft > 64 || vocab < 1 || vocab >= ((int64_t)1 << 31))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!p || !v || !out || !n_out || (num_draft > 0 && (!q || !draft || !u))) return PA_ERR_INVALID_ARG;
+    const void *ptrs[] = {p, q, draft, u, v, out, n_out};
+    for (const void *x : ptrs)
+        if (reinterpret_cast<uintptr_t>(x) & 3u) return PA_ERR_INVALID_ARG;
+    return launch_spec_verify(p, q, draft, u, v, num_seqs, num_draft, vocab, out, n_out, nullptr,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_pool_selftest_wait(pa_pool *pool, uint64_t limit_ns, void *stream) {
     if (!pool || limit_ns > 10ull * 1000000000ull) return PA_ERR_INVALID_ARG;
     DeviceGuard g(pool->cfg.device);

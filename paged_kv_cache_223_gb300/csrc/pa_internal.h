@@ -61,6 +61,11 @@ cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const 
                           const CUtensorMap &tmv, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
+                               int B, int K, int64_t V, int32_t *out, int32_t *n_out, int *status,
+                               cudaStream_t stream);
+cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n, void *k_cache, void *v_cache, int64_t vec_per_block,
+                               int32_t num_blocks, int *status, int sm_count, cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int nt);
 size_t merge_smem_bytes(int G, int max_parts, int head_dim);
 constexpr size_t MAX_SMEM_PER_CTA = 227 * 1024;

@@ -210,3 +210,127 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     return L.pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, d, _PA_DTYPE[q.dtype],
                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, q_len,
                                float(scale), partition_tokens, _ptr(out), _stream(stream))
+
+
+# ------------------------------------------------------------------------------ block manager
+
+_alloc_ready = False
+
+
+def _alloc_lib() -> C.CDLL:
+    global _alloc_ready
+    L = lib()
+    if not _alloc_ready:
+        P, I32 = C.c_void_p, C.c_int32
+        L.pa_allocator_create.argtypes = [I32, I32, C.POINTER(C.c_void_p)]
+        L.pa_allocator_destroy.argtypes = [P]
+        L.pa_allocator_destroy.restype = None
+        L.pa_allocator_num_free.argtypes = [P]
+        L.pa_allocator_num_free.restype = I32
+        L.pa_allocator_ref_count.argtypes = [P, I32]
+        L.pa_allocator_ref_count.restype = I32
+        L.pa_allocator_alloc.argtypes = [P, I32, P]
+        L.pa_allocator_fork.argtypes = [P, P, I32]
+        L.pa_allocator_free.argtypes = [P, P, I32]
+        L.pa_allocator_cow.argtypes = [P, I32, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+        L.pa_allocator_append.argtypes = [P, P, I32, C.POINTER(C.c_int32), I32, P, P, C.POINTER(C.c_int32)]
+        L.pa_copy_blocks.argtypes = [P, P, I32, P, P, P]
+        for f in ("pa_allocator_create", "pa_allocator_alloc", "pa_allocator_fork", "pa_allocator_free",
+                  "pa_allocator_cow", "pa_allocator_append", "pa_copy_blocks"):
+            getattr(L, f).restype = C.c_int
+        _alloc_ready = True
+    return L
+
+
+class BlockAllocator:
+    """Host-side free pool with reference counts and copy-on-write (pa_allocator_*). No GPU needed."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        import numpy as np
+        self._np = np
+        self.block_size = block_size
+        h = C.c_void_p()
+        _check(_alloc_lib().pa_allocator_create(num_blocks, block_size, C.byref(h)), "pa_allocator_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _alloc_lib().pa_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _ids(self, ids):
+        return self._np.ascontiguousarray(ids, dtype=self._np.int32)
+
+    @property
+    def num_free(self) -> int:
+        return _alloc_lib().pa_allocator_num_free(self._h)
+
+    def ref_count(self, block_id: int) -> int:
+        return _alloc_lib().pa_allocator_ref_count(self._h, block_id)
+
+    def alloc(self, n: int):
+        out = self._np.empty(n, dtype=self._np.int32)
+        _check(_alloc_lib().pa_allocator_alloc(self._h, n, out.ctypes.data), "pa_allocator_alloc")
+        return out
+
+    def fork(self, ids) -> None:
+        a = self._ids(ids)
+        _check(_alloc_lib().pa_allocator_fork(self._h, a.ctypes.data, len(a)), "pa_allocator_fork")
+
+    def free(self, ids) -> None:
+        a = self._ids(ids)
+        _check(_alloc_lib().pa_allocator_free(self._h, a.ctypes.data, len(a)), "pa_allocator_free")
+
+    def cow(self, block_id: int):
+        out, copy = C.c_int32(), C.c_int32()
+        _check(_alloc_lib().pa_allocator_cow(self._h, block_id, C.byref(out), C.byref(copy)), "pa_allocator_cow")
+        return out.value, bool(copy.value)
+
+    def append(self, table_row, length: int, n_new: int):
+        """Extend a sequence by n_new tokens. table_row: int32 numpy row, updated in place.
+        Returns (slots int64[n_new], new length, copy pair or None)."""
+        assert table_row.dtype == self._np.int32 and table_row.flags.c_contiguous
+        slots = self._np.empty(n_new, dtype=self._np.int64)
+        pair = self._np.empty(2, dtype=self._np.int32)
+        ln, nc = C.c_int32(length), C.c_int32()
+        _check(_alloc_lib().pa_allocator_append(self._h, table_row.ctypes.data, len(table_row), C.byref(ln), n_new,
+                                                slots.ctypes.data, pair.ctypes.data, C.byref(nc)), "pa_allocator_append")
+        return slots, ln.value, (tuple(int(x) for x in pair) if nc.value else None)
+
+
+def copy_blocks(pool: "Pool", pairs: torch.Tensor, k_cache: Optional[torch.Tensor] = None,
+                v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """pa_copy_blocks: copy whole blocks pairs[i, 0] -> pairs[i, 1] (device int32 [n, 2])."""
+    _dev(pairs, "pairs", torch.int32)
+    _check(_alloc_lib().pa_copy_blocks(pool.handle, _ptr(pairs), pairs.shape[0], _ptr(k_cache), _ptr(v_cache),
+                                       _stream(stream)), "pa_copy_blocks")
+
+
+_spec_ready = False
+
+
+def spec_verify(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u: torch.Tensor, v: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None):
+    """pa_spec_verify: speculative rejection sampling. Returns (out int32 [B, K+1], n_out int32 [B])."""
+    global _spec_ready
+    L = lib()
+    if not _spec_ready:
+        P, I32 = C.c_void_p, C.c_int32
+        L.pa_spec_verify.argtypes = [P, P, P, P, P, I32, I32, C.c_int64, P, P, P]
+        L.pa_spec_verify.restype = C.c_int
+        _spec_ready = True
+    for name, t, dt in (("p", p, torch.float32), ("q", q, torch.float32), ("draft", draft, torch.int32),
+                        ("u", u, torch.float32), ("v", v, torch.float32)):
+        _dev(t, name, dt)
+    B, K1, V = p.shape
+    out = torch.empty((B, K1), dtype=torch.int32, device=p.device)
+    n_out = torch.empty((B,), dtype=torch.int32, device=p.device)
+    _check(L.pa_spec_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), _ptr(v), B, K1 - 1, V, _ptr(out), _ptr(n_out),
+                            _stream(stream)), "pa_spec_verify")
+    return out, n_out
