@@ -66,6 +66,15 @@ def lib():
                                                       C.c_int, C.c_float, C.c_int64, P, P, P]
             L.oracle_lse_merge.argtypes = [C.c_int64, P, P, P, C.c_int, P]
             L.oracle_spec_verify.argtypes = [P, P, P, P, P, C.c_int64, C.c_int, C.c_int64, P, P]
+            L.oracle_e4m3_to_double.argtypes = [C.c_uint8]
+            L.oracle_e4m3_to_double.restype = C.c_double
+            L.oracle_f32_to_e4m3.argtypes = [C.c_float]
+            L.oracle_f32_to_e4m3.restype = C.c_uint8
+            L.oracle_cache_write_fp8.argtypes = [P, P, P, P, P, C.c_int64, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int]
+            L.oracle_cache_write_fp8.restype = C.c_int
+            L.oracle_paged_attention_fp8.argtypes = [P, P, P, P, C.c_int64, P, P, C.c_int, C.c_int64, C.c_int, C.c_int,
+                                                     C.c_int, C.c_int, C.c_int, C.c_int, C.c_float, P]
+            L.oracle_paged_attention_fp8.restype = C.c_int
             L.oracle_num_cpus.argtypes = []
             for f in ("oracle_cache_write", "oracle_gather", "oracle_copy_blocks", "oracle_attention", "oracle_paged_attention",
                       "oracle_attention_partitions", "oracle_lse_merge", "oracle_num_cpus", "oracle_spec_verify"):
@@ -202,3 +211,50 @@ def spec_verify(p: np.ndarray, q: np.ndarray, draft: np.ndarray, u: np.ndarray, 
     _check(lib().oracle_spec_verify(_p(p), _p(q), _p(draft), _p(u), _p(v), B, K1 - 1, V, _p(out), _p(n)),
            "spec_verify")
     return out, n
+
+
+# ------------------------------------------------------------------------------ FP8 KV
+
+def e4m3_to_double(c: int) -> float:
+    return lib().oracle_e4m3_to_double(c)
+
+
+def f32_to_e4m3(x: float) -> int:
+    return lib().oracle_f32_to_e4m3(x)
+
+
+def fp8_pool(num_blocks: int, Hkv: int, bs: int, d: int, fill_code: int = 0) -> np.ndarray:
+    """An FP8 pool buffer: codes [NB, Hkv, bs, d] then float32 scales [NB, Hkv, bs], as one byte array."""
+    codes = num_blocks * Hkv * bs * d
+    buf = np.zeros(codes + 4 * num_blocks * Hkv * bs, dtype=np.uint8)
+    buf[:codes] = fill_code
+    return buf
+
+
+def fp8_views(buf: np.ndarray, num_blocks: int, Hkv: int, bs: int, d: int):
+    codes = num_blocks * Hkv * bs * d
+    return buf[:codes].reshape(num_blocks, Hkv, bs, d), buf[codes:].view(np.float32).reshape(num_blocks, Hkv, bs)
+
+
+def cache_write_fp8(k_buf: np.ndarray, v_buf: np.ndarray, geometry, k: np.ndarray, v: np.ndarray,
+                    slot_mapping: np.ndarray, dtype: int) -> None:
+    NB, Hkv, bs, d = geometry
+    k, v = _u16(k), _u16(v)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    _check(lib().oracle_cache_write_fp8(_p(k_buf), _p(v_buf), _p(k), _p(v), _p(sm), len(sm), NB, bs, Hkv, d, dtype),
+           "cache_write_fp8")
+
+
+def paged_attention_fp8(q: np.ndarray, k_buf: np.ndarray, v_buf: np.ndarray, geometry, block_tables: np.ndarray,
+                        context_lens: np.ndarray, dtype: int, scale: float, seqs=None) -> np.ndarray:
+    NB, Hkv, bs, d = geometry
+    q = _u16(q)
+    n, q_len, Hq, _ = q.shape
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    sq = None if seqs is None else np.ascontiguousarray(seqs, dtype=np.int32)
+    out = np.empty((n, q_len, Hq, d), dtype=np.float64)
+    _check(lib().oracle_paged_attention_fp8(_p(q), _p(k_buf), _p(v_buf), _p(tables), tables.shape[1], _p(lens), _p(sq),
+                                            n, NB, bs, q_len, Hq, Hkv, d, dtype, scale, _p(out)),
+           "paged_attention_fp8")
+    return out

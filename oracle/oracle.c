@@ -154,28 +154,26 @@ int oracle_gather(const uint16_t *pool, const int32_t *table_row, int64_t L, int
 /* --------------------------------------------------------------- attention */
 
 /*
- * One sequence on contiguous K/V.
- *   q   [q_len, Hq, d]     kc, vc  [L, Hkv, d]     out  [q_len, Hq, d] (double)
+ * The attention of one sequence on contiguous K/V given as fp64 values.
+ *   qd  [q_len, Hq, d]     kd, vd  [L, Hkv, d]     out  [q_len, Hq, d]
  *   weights (optional) [q_len, Hq, L]: the softmax weights, 0 for masked tokens.
  */
-int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int64_t L, int q_len,
-                     int Hq, int Hkv, int d, int dtype, float scale, double *out, double *weights) {
-    if (!q || !kc || !vc || !out || q_len < 1 || L < q_len || Hkv <= 0 || Hq % Hkv != 0 || d <= 0)
-        return OR_ERR_ARG;
+static int attention_f64(const double *qd, const double *kd, const double *vd, int64_t L, int q_len, int Hq,
+                         int Hkv, int d, float scale, double *out, double *weights) {
+    if (q_len < 1 || L < q_len || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return OR_ERR_ARG;
     int G = Hq / Hkv;
     double *s = (double *)malloc((size_t)L * sizeof(double));
-    double *qd = (double *)malloc((size_t)d * sizeof(double));
-    if (!s || !qd) { free(s); free(qd); return OR_ERR_OOM; }
+    if (!s) return OR_ERR_OOM;
     for (int qi = 0; qi < q_len; ++qi) {
         int64_t last = L - q_len + qi;                     /* inclusive causal limit */
         for (int h = 0; h < Hq; ++h) {
             int g = h / G;
-            for (int k = 0; k < d; ++k) qd[k] = dec(q[((int64_t)qi * Hq + h) * d + k], dtype);
+            const double *qr = qd + ((int64_t)qi * Hq + h) * d;
             double mx = -INFINITY;
             for (int64_t t = 0; t <= last; ++t) {
                 double dot = 0.0;
-                const uint16_t *kr = kc + (t * Hkv + g) * (int64_t)d;
-                for (int k = 0; k < d; ++k) dot += qd[k] * dec(kr[k], dtype);
+                const double *kr = kd + (t * Hkv + g) * (int64_t)d;
+                for (int k = 0; k < d; ++k) dot += qr[k] * kr[k];
                 s[t] = (double)scale * dot;
                 if (s[t] > mx) mx = s[t];
             }
@@ -185,8 +183,8 @@ int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, 
             for (int k = 0; k < d; ++k) o[k] = 0.0;
             for (int64_t t = 0; t <= last; ++t) {
                 double p = s[t] / l;
-                const uint16_t *vr = vc + (t * Hkv + g) * (int64_t)d;
-                for (int k = 0; k < d; ++k) o[k] += p * dec(vr[k], dtype);
+                const double *vr = vd + (t * Hkv + g) * (int64_t)d;
+                for (int k = 0; k < d; ++k) o[k] += p * vr[k];
             }
             if (weights) {
                 double *w = weights + ((int64_t)qi * Hq + h) * L;
@@ -195,8 +193,34 @@ int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, 
         }
     }
     free(s);
-    free(qd);
     return OR_OK;
+}
+
+static double *decode_all(const uint16_t *w, int64_t n, int dtype) {
+    double *x = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (x)
+        for (int64_t i = 0; i < n; ++i) x[i] = dec(w[i], dtype);
+    return x;
+}
+
+/*
+ * One sequence on contiguous K/V (16-bit words, decoded exactly).
+ *   q   [q_len, Hq, d]     kc, vc  [L, Hkv, d]     out  [q_len, Hq, d] (double)
+ *   weights (optional) [q_len, Hq, L]: the softmax weights, 0 for masked tokens.
+ */
+int oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int64_t L, int q_len,
+                     int Hq, int Hkv, int d, int dtype, float scale, double *out, double *weights) {
+    if (!q || !kc || !vc || !out || q_len < 1 || L < q_len || Hkv <= 0 || Hq % Hkv != 0 || d <= 0)
+        return OR_ERR_ARG;
+    double *qd = decode_all(q, (int64_t)q_len * Hq * d, dtype);
+    double *kd = decode_all(kc, L * Hkv * d, dtype);
+    double *vd = decode_all(vc, L * Hkv * d, dtype);
+    int rc = (!qd || !kd || !vd) ? OR_ERR_OOM
+                                 : attention_f64(qd, kd, vd, L, q_len, Hq, Hkv, d, scale, out, weights);
+    free(qd);
+    free(kd);
+    free(vd);
+    return rc;
 }
 
 /* --------------------------------------------------------- paged attention */
@@ -481,4 +505,152 @@ int oracle_spec_verify(const float *p, const float *q, const int32_t *draft, con
     }
     free(w);
     return rc;
+}
+
+/* ---------------------------------------------------------------- FP8 KV */
+
+/*
+ * FP8 E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 fraction bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448): the code's value.
+ */
+double oracle_e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                  /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Round a float to the nearest E4M3 value (ties to even), saturating to +-448; NaN -> NaN code. */
+uint8_t oracle_f32_to_e4m3(float x) {
+    if (x != x) return 0x7F;
+    uint8_t sign = (x < 0.0f || (x == 0.0f && 1.0f / x < 0.0f)) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    /* quantum of the binade (normals: 2^(e-3); subnormals: 2^-9) */
+    int e;
+    frexp(a, &e);                                   /* a = f * 2^e, f in [0.5, 1) -> binade exponent e-1 */
+    int be = e - 1;
+    if (be < -6) be = -6;
+    double quantum = ldexp(1.0, be - 3);
+    double n = nearbyint(a / quantum);              /* exact division by a power of two; ties to even */
+    double r = n * quantum;
+    if (r >= 448.0) return sign | 0x7E;
+    if (r == 0.0) return sign;
+    int re;
+    frexp(r, &re);
+    int rbe = re - 1;                               /* binade of the rounded value */
+    if (rbe < -6) {                                 /* subnormal: r = m * 2^-9 */
+        int m = (int)nearbyint(r / ldexp(1.0, -9));
+        return sign | (uint8_t)m;
+    }
+    int m = (int)nearbyint(r / ldexp(1.0, rbe - 3)) - 8;
+    return sign | (uint8_t)(((rbe + 7) << 3) | m);
+}
+
+/*
+ * Quantising cache write. A pool in FP8 layout holds, in one buffer, the codes
+ * [num_blocks, Hkv, bs, d] (bytes) followed by one float32 scale per slot and
+ * head [num_blocks, Hkv, bs]. Each new (token, head) row of d 16-bit values x
+ * is stored as scale = amax|x| / 448 (float32; 1 when amax is 0) and codes
+ * e4m3(x / scale) (the division in float32), so the row's largest magnitude
+ * maps to the largest finite code and nothing overflows (the quantisation
+ * section of learn.tanhdev.com part 8: FP8 E4M3 KV halves the cache, with care
+ * against outliers; yangyu.win blog #54 section 4: quantise the KV cache to
+ * FP8). slot < 0 is skipped.
+ */
+int oracle_cache_write_fp8(uint8_t *k_pool, uint8_t *v_pool, const uint16_t *k, const uint16_t *v,
+                           const int64_t *slot_mapping, int64_t num_tokens, int64_t num_blocks, int bs, int Hkv,
+                           int d, int dtype) {
+    if (!k_pool || !v_pool || !k || !v || !slot_mapping || bs <= 0 || Hkv <= 0 || d <= 0) return OR_ERR_ARG;
+    const int64_t codes = num_blocks * Hkv * bs * (int64_t)d;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        int64_t blk = s / bs, off = s % bs;
+        if (blk >= num_blocks) return OR_ERR_BOUNDS;
+        for (int which = 0; which < 2; ++which) {
+            uint8_t *pool = which ? v_pool : k_pool;
+            const uint16_t *src = which ? v : k;
+            float *scales = (float *)(pool + codes);
+            for (int h = 0; h < Hkv; ++h) {
+                const uint16_t *row = src + (i * Hkv + h) * (int64_t)d;
+                float amax = 0.0f;
+                for (int c = 0; c < d; ++c) {
+                    float a = fabsf((float)dec(row[c], dtype));
+                    if (a > amax) amax = a;
+                }
+                float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+                int64_t slot_row = (blk * Hkv + h) * bs + off;
+                scales[slot_row] = scale;
+                for (int c = 0; c < d; ++c) pool[slot_row * d + c] = oracle_f32_to_e4m3((float)dec(row[c], dtype) / scale);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Paged decode over FP8 pools: each (sequence, KV head) item gathers its codes
+ * and scales through the block table, dequantises (code value * scale, fp64)
+ * and runs the same attention as the 16-bit path. q and out as in
+ * oracle_paged_attention.
+ */
+int oracle_paged_attention_fp8(const uint16_t *q, const uint8_t *k_pool, const uint8_t *v_pool,
+                               const int32_t *block_tables, int64_t stride, const int32_t *context_lens,
+                               const int32_t *seqs, int nseq, int64_t num_blocks, int bs, int q_len, int Hq,
+                               int Hkv, int d, int dtype, float scale, double *out) {
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || nseq < 0 || Hkv <= 0 ||
+        Hq % Hkv != 0)
+        return OR_ERR_ARG;
+    const int G = Hq / Hkv;
+    const int64_t codes = num_blocks * Hkv * bs * (int64_t)d;
+    const float *ks = (const float *)(k_pool + codes);
+    const float *vs = (const float *)(v_pool + codes);
+    for (int i = 0; i < nseq; ++i) {
+        const int b = seqs ? seqs[i] : i;
+        const int64_t L = context_lens[b];
+        if (L < q_len || (L + bs - 1) / bs > stride) return OR_ERR_BOUNDS;
+        const int32_t *row = block_tables + (int64_t)b * stride;
+        double *qd = (double *)malloc((size_t)q_len * G * d * sizeof(double));
+        double *kd = (double *)malloc((size_t)L * d * sizeof(double));
+        double *vd = (double *)malloc((size_t)L * d * sizeof(double));
+        double *od = (double *)malloc((size_t)q_len * G * d * sizeof(double));
+        int rc = (!qd || !kd || !vd || !od) ? OR_ERR_OOM : OR_OK;
+        for (int g = 0; g < Hkv && rc == OR_OK; ++g) {
+            for (int64_t t = 0; t < L && rc == OR_OK; ++t) {
+                int64_t phys = row[t / bs];
+                if (phys < 0 || phys >= num_blocks) { rc = OR_ERR_BOUNDS; break; }
+                int64_t sr = (phys * Hkv + g) * bs + t % bs;
+                for (int c = 0; c < d; ++c) {
+                    kd[t * d + c] = oracle_e4m3_to_double(k_pool[sr * d + c]) * (double)ks[sr];
+                    vd[t * d + c] = oracle_e4m3_to_double(v_pool[sr * d + c]) * (double)vs[sr];
+                }
+            }
+            if (rc != OR_OK) break;
+            const uint16_t *qb = q + (int64_t)i * q_len * Hq * d;
+            for (int qi = 0; qi < q_len; ++qi)
+                for (int hh = 0; hh < G; ++hh)
+                    for (int c = 0; c < d; ++c)
+                        qd[((int64_t)qi * G + hh) * d + c] = dec(qb[((int64_t)qi * Hq + g * G + hh) * d + c], dtype);
+            rc = attention_f64(qd, kd, vd, L, q_len, G, 1, d, scale, od, NULL);
+            double *ob = out + (int64_t)i * q_len * Hq * d;
+            for (int qi = 0; qi < q_len && rc == OR_OK; ++qi)
+                for (int hh = 0; hh < G; ++hh)
+                    memcpy(ob + ((int64_t)qi * Hq + g * G + hh) * d, od + ((int64_t)qi * G + hh) * d,
+                           (size_t)d * sizeof(double));
+        }
+        free(qd);
+        free(kd);
+        free(vd);
+        free(od);
+        if (rc != OR_OK) return rc;
+    }
+    return OR_OK;
 }

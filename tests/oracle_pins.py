@@ -431,8 +431,98 @@ def pin_spec_verify_special_cases():
     assert (r[np.arange(B), out[:, 0]] > 0).all()
 
 
+def _torch_e4m3_values():
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_decode_matches_torch():
+    ref = _torch_e4m3_values()
+    got = np.array([oracle.e4m3_to_double(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+    assert np.nanmax(got) == 448.0 and got[1] == 2.0 ** -9
+
+
+def pin_e4m3_encode_matches_torch():
+    rng = _rng(13)
+    x = np.concatenate([rng.uniform(-464, 464, 4000), rng.standard_normal(4000) * 3, rng.standard_normal(2000) * 0.01,
+                        (_torch_e4m3_values()[:126] * np.array([1.0])), [0.0, -0.0, 2 ** -10, 3 * 2 ** -11, 1.0625,
+                                                                       1.1875, 448.0, 464.0, -464.0]]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f32_to_e4m3(float(v)) for v in x], dtype=np.uint8)
+    zero = (x == 0)
+    assert np.array_equal(got[~zero], ref[~zero])
+    assert all(oracle.f32_to_e4m3(v) == 0x7E for v in (465.0, 1e6)) and oracle.f32_to_e4m3(-1e30) == 0xFE
+
+
+def pin_fp8_quantised_write_bounds():
+    """Each (token, head) row maps its largest magnitude to 448; every value is within half a quantum."""
+    rng = _rng(14)
+    NB, Hkv, bs, d, dt = 4, 2, 16, 64, BF16
+    kbuf, vbuf = oracle.fp8_pool(NB, Hkv, bs, d), oracle.fp8_pool(NB, Hkv, bs, d)
+    k = words(rng, (10, Hkv, d), dt, sigma=2.0)
+    v = words(rng, (10, Hkv, d), dt, sigma=0.01)
+    slots = np.array([3, 17, 18, 40, 63, 0, 5, 6, 33, 34])
+    oracle.cache_write_fp8(kbuf, vbuf, (NB, Hkv, bs, d), k, v, slots, dt)
+    vals = _torch_e4m3_values()
+    for buf, src in ((kbuf, k), (vbuf, v)):
+        codes, scales = oracle.fp8_views(buf, NB, Hkv, bs, d)
+        x = lib_decode(src, dt)
+        for i, sl in enumerate(slots):
+            for h in range(Hkv):
+                sc = scales[sl // bs, h, sl % bs]
+                assert sc == np.float32(np.float32(np.abs(x[i, h]).max()) / np.float32(448.0))
+                deq = vals[codes[sl // bs, h, sl % bs]] * np.float64(sc)
+                assert np.abs(vals[codes[sl // bs, h, sl % bs]]).max() == 448.0
+                assert (np.abs(deq - x[i, h]) <= np.maximum(np.abs(x[i, h]) * 2.0 ** -4, float(sc) * 2.0 ** -10) * 1.0000001).all()
+
+
+def pin_fp8_attention_matches_sdpa():
+    """The FP8 paged chain (quantising write, gather, dequantise, attention) == torch fp64 SDPA on the
+    dequantised K/V."""
+    rng = _rng(15)
+    NB, Hkv, bs, d, Hq, dt = 12, 2, 16, 32, 8, FP16
+    lens = np.array([5, 37, 90], np.int32)
+    tables = np.full((3, 6), -1, np.int32)
+    perm = rng.permutation(NB)
+    kbuf, vbuf = oracle.fp8_pool(NB, Hkv, bs, d), oracle.fp8_pool(NB, Hkv, bs, d)
+    pos, ks, vs = 0, [], []
+    for b, L in enumerate(lens):
+        nb = -(-int(L) // bs)
+        tables[b, :nb] = perm[pos:pos + nb]
+        pos += nb
+        k, v = words(rng, (int(L), Hkv, d), dt), words(rng, (int(L), Hkv, d), dt)
+        t = np.arange(L)
+        oracle.cache_write_fp8(kbuf, vbuf, (NB, Hkv, bs, d), k, v, tables[b, t // bs].astype(np.int64) * bs + t % bs, dt)
+        ks.append(k)
+        vs.append(v)
+    for ql in (1, 5):
+        q = words(rng, (3, ql, Hq, d), dt)
+        scale = float(np.float32(0.2))
+        out = oracle.paged_attention_fp8(q, kbuf, vbuf, (NB, Hkv, bs, d), tables, lens, dt, scale)
+        vals = _torch_e4m3_values()
+        kc, ksc = oracle.fp8_views(kbuf, NB, Hkv, bs, d)
+        vc, vsc = oracle.fp8_views(vbuf, NB, Hkv, bs, d)
+        for b, L in enumerate(lens):
+            if L < ql:
+                continue
+            t = np.arange(L)
+            pb, off = tables[b, t // bs], t % bs
+            kd = vals[kc[pb, :, off]] * ksc[pb, :, off][..., None].astype(np.float64)
+            vd = vals[vc[pb, :, off]] * vsc[pb, :, off][..., None].astype(np.float64)
+            qf = np.zeros((L, Hq, d))
+            qf[L - ql:] = lib_decode(q[b], dt)
+            Q = torch.from_numpy(qf).permute(1, 0, 2)[None]
+            K = torch.from_numpy(kd).permute(1, 0, 2)[None]
+            V = torch.from_numpy(vd).permute(1, 0, 2)[None]
+            ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=scale,
+                                                                   enable_gqa=True)[0].permute(1, 0, 2).numpy()[L - ql:]
+            assert np.allclose(out[b], ref, rtol=1e-10, atol=1e-12)
+
+
 ALL_PINS = [pin_decode_fp16, pin_decode_bf16, pin_mapping_yangyu, pin_mapping_tanhdev, pin_kv_size_closed_form,
             pin_sdpa_contiguous, pin_paged_equals_contiguous_under_permutation, pin_closed_forms, pin_weights,
             pin_gqa_is_mha_with_duplicated_heads, pin_verify_rows_are_decodes, pin_shared_prefix_equals_duplicated,
             pin_split_merge_equals_unsplit, pin_cache_write_skip_and_untouched, pin_copy_on_write_equals_private_write,
-            pin_spec_verify_is_lossless, pin_spec_verify_special_cases]
+            pin_spec_verify_is_lossless, pin_spec_verify_special_cases, pin_e4m3_decode_matches_torch,
+            pin_e4m3_encode_matches_torch, pin_fp8_quantised_write_bounds, pin_fp8_attention_matches_sdpa]

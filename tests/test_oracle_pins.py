@@ -16,8 +16,8 @@ import oracle_pins as pins
 
 MUTANTS = {
     "drop_scale": ("s[t] = (double)scale * dot;", "s[t] = dot;"),
-    "gqa_modulo": ("            int g = h / G;\n            for (int k = 0; k < d; ++k) qd[k]",
-                   "            int g = h % Hkv;\n            for (int k = 0; k < d; ++k) qd[k]"),
+    "gqa_modulo": ("            int g = h / G;\n            const double *qr = qd",
+                   "            int g = h % Hkv;\n            const double *qr = qd"),
     "no_causal_limit": ("        int64_t last = L - q_len + qi;                     /* inclusive causal limit */",
                         "        int64_t last = L - 1;"),
     "causal_off_by_one": ("        int64_t last = L - q_len + qi;                     /* inclusive causal limit */",
@@ -28,8 +28,8 @@ MUTANTS = {
     "group_query_wrong_head": ("qb + ((int64_t)qi * J->Hq + g * G + hh) * J->d", "qb + ((int64_t)qi * J->Hq + hh) * J->d"),
     "group_out_wrong_row": ("ob + ((int64_t)qi * J->Hq + g * G + hh) * J->d", "ob + ((int64_t)qi * J->Hq + hh * J->Hkv + g) * J->d"),
     "no_normalise": ("double p = s[t] / l;", "double p = s[t];"),
-    "dot_reads_v": ("const uint16_t *kr = kc + (t * Hkv + g) * (int64_t)d;\n                for (int k = 0; k < d; ++k) dot += qd[k]",
-                    "const uint16_t *kr = vc + (t * Hkv + g) * (int64_t)d;\n                for (int k = 0; k < d; ++k) dot += qd[k]"),
+    "dot_reads_v": ("const double *kr = kd + (t * Hkv + g) * (int64_t)d;",
+                    "const double *kr = vd + (t * Hkv + g) * (int64_t)d;"),
     "no_max_shift_bug": ("{ s[t] = exp(s[t] - mx); l += s[t]; }", "{ s[t] = exp(s[t] - mx); l += 1.0; }"),
     "cache_write_offset": ("int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = 0;"),
     "cache_write_head_swap": ("int64_t dst = ((blk * Hkv + h) * bs + off) * (int64_t)d;",
@@ -49,6 +49,11 @@ MUTANTS = {
     "spec_accept_inverted": ("if (uq < pi) {", "if (uq > pi) {"),
     "spec_bonus_wrong_row": ("const float *pr = p + (b * (K + 1) + K) * V;", "const float *pr = p + (b * (K + 1) + K - 1) * V;"),
     "spec_cdf_off_by_one": ("if (c > target) return t;", "if (c > target) return t > 0 ? t - 1 : 0;"),
+    "e4m3_bias": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 9);"),
+    "e4m3_round_down": ("double n = nearbyint(a / quantum);", "double n = floor(a / quantum);"),
+    "fp8_scale_max": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;", "float scale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    "fp8_dequant_no_scale": ("kd[t * d + c] = oracle_e4m3_to_double(k_pool[sr * d + c]) * (double)ks[sr];",
+                             "kd[t * d + c] = oracle_e4m3_to_double(k_pool[sr * d + c]);"),
     "weights_unmasked": ("w[t] = t <= last ? s[t] / l : 0.0;", "w[t] = t <= last ? s[t] / l : 1e-300;"),
 }
 
