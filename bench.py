@@ -141,16 +141,16 @@ class ClockSampler:
 class GpuWorkload:
     """Every layer's pool filled through pa_cache_write; per-layer inputs resident on the device."""
 
-    def __init__(self, wl: synth.Workload, dev):
+    def __init__(self, wl: synth.Workload, dev, kv_format: int = 0):
         import torch
         import gpu_harness as H
         import synth.device as sdev
         self.wl = wl
         self.layers = []
-        kc0, vc0 = H.alloc_caches(wl)
-        self.pool = H.make_pool(wl, 0, kc0, vc0)
+        kc0, vc0 = H.alloc_caches(wl, kv_format)
+        self.pool = H.make_pool(wl, 0, kc0, vc0, kv_format=kv_format)
         for layer in range(wl.layers):
-            kc, vc = (kc0, vc0) if layer == 0 else H.alloc_caches(wl)
+            kc, vc = (kc0, vc0) if layer == 0 else H.alloc_caches(wl, kv_format)
             H.fill(self.pool, wl, layer, kc, vc, new_only=False)
             lw = synth.with_layer(wl, layer)
             (kind, rows, slots), = lw.write_plan(new_only=True)
@@ -192,12 +192,16 @@ def job_value(bytes_per_rank_step: int, steps: int, elapsed_ms: float, world_siz
     return world_size * bytes_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e9
 
 
-def step_bytes(wl: synth.Workload):
+def step_bytes(wl: synth.Workload, kv_format: int = 0):
     """Algorithmic bytes of one step: per layer, the decode's (q + unique valid K/V + used table entries + lens + out)
-    and the cache write's (new k/v read + slot map + the rows written)."""
+    and the cache write's (new k/v read + slot map + the rows written). FP8 pools store d code bytes plus a
+    4-byte scale per (token, head) row instead of 2*d bytes."""
     n_new = wl.B * wl.q_len
-    cw = 2 * n_new * wl.Hkv * wl.d * 2 * 2 + 8 * n_new
-    return wl.layers * (wl.algorithmic_bytes() + cw), wl.algorithmic_bytes()
+    row16 = wl.d * 2
+    row = wl.d + 4 if kv_format else row16
+    dec = wl.algorithmic_bytes() - wl.kv_bytes_unique() + wl.kv_bytes_unique() // row16 * row
+    cw = n_new * wl.Hkv * 2 * (row16 + row) + 8 * n_new
+    return wl.layers * (dec + cw), dec
 
 
 def run_gpu(args):
@@ -210,8 +214,9 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     k = WORKLOADS[args.workload]
     wl = synth.workload(k, layers=args.layers, batch=args.batch)
-    G = GpuWorkload(wl, dev)
-    total_bytes, decode_bytes = step_bytes(wl)
+    kv_format = 1 if args.kv == "fp8" else 0
+    G = GpuWorkload(wl, dev, kv_format)
+    total_bytes, decode_bytes = step_bytes(wl, kv_format)
     kv_tokens = int(wl.context_lens.sum()) * wl.layers
 
     def barrier():
@@ -246,7 +251,7 @@ def run_gpu(args):
     value = job_value(total_bytes, args.steps, elapsed_ms, ws)
 
     # end to end through the public API: pinned host inputs -> device, kernels, result -> host
-    e2e = None if args.no_e2e else run_e2e(G, wl, dev, max(3, args.steps // 5), barrier)
+    e2e = None if args.no_e2e else run_e2e(G, wl, dev, max(3, args.steps // 5), barrier, kv_format)
 
     if rank == 0:
         peak, peak_kind = peaks()
@@ -256,13 +261,16 @@ def run_gpu(args):
             "metric": "paged-attn decode KV GB/s & KV tokens/s on 1 GB300 (fraction of HBM peak)",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp16" if wl.dtype == synth.FP16 else "bf16", "data": "synthetic (seeded, N(0,1)-shaped)",
+            "dtype": ("fp16" if wl.dtype == synth.FP16 else "bf16") + ("+fp8-kv" if kv_format else ""),
+            "data": "synthetic (seeded, N(0,1)-shaped)",
             "config": {**synth.describe(wl), "workload": f"{args.workload}: {DESCR[k]}",
+                       "kv_cache": "fp8 e4m3 + fp32 scale per (slot, head)" if kv_format else "16-bit",
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{ws}"},
             "kv_tokens_per_s": round(ws * kv_tokens * args.steps / (elapsed_ms * 1e-3), 1),
             "fraction_of_hbm_peak": round(value / peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.workload),
+                         "frac": round(achieved / peak, 4),
+                         "traffic": None if kv_format else measured_traffic(args.workload),
                          "kernel": "pa_decode call (decode kernel + partition merge)",
                          "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                          "peak_kind": peak_kind},
@@ -270,14 +278,14 @@ def run_gpu(args):
             "gpu_launches": G.launches_per_step() * args.steps,
             "clocks": clk.summary(),
         }
-        if ws == 1 and not args.no_cpu_baseline:
+        if ws == 1 and not args.no_cpu_baseline and not kv_format:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier):
+def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier, kv_format: int = 0):
     """Same step through the Python binding with per-step inputs copied from pinned host memory and the outputs
     read back, all inside the timed region."""
     import torch
@@ -304,7 +312,7 @@ def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier):
         one()
     barrier()
     dt = (time.perf_counter() - t0) / steps
-    total_bytes, _ = step_bytes(wl)
+    total_bytes, _ = step_bytes(wl, kv_format)
     ws = dist_env()[0]
     return {"value": round(ws * total_bytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3), "steps": steps}
@@ -418,6 +426,7 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"], help="KV cache storage")
     ap.add_argument("--layers", type=int, default=None, help="layer pools (workload 3 only; default 80)")
     ap.add_argument("--batch", type=int, default=None, help="sequences (default: the workload's)")
     args = ap.parse_args()

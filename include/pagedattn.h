@@ -50,6 +50,18 @@ typedef enum pa_status {
 
 typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
 
+/*
+ * How K and V are stored in the pool.
+ *  PA_KV_16BIT     in the model dtype: each cache is [num_blocks, Hkv, bs, head_dim] 16-bit values.
+ *  PA_KV_FP8_E4M3  FP8 E4M3 codes with one float32 scale per (slot, head): each cache is one buffer
+ *                  of num_blocks*Hkv*bs*head_dim code bytes followed by num_blocks*Hkv*bs float32
+ *                  scales ([num_blocks, Hkv, bs]). pa_cache_write quantises: scale = amax|row| / 448
+ *                  (1 for an all-zero row), code = e4m3(x / scale), nearest even, saturated; decode
+ *                  uses code * scale. head_dim 128 only. (yangyu.win blog #54 section 4 and the
+ *                  quantisation section of learn.tanhdev.com part 8: FP8 E4M3 halves the KV cache.)
+ */
+typedef enum pa_kv_format { PA_KV_16BIT = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_format;
+
 typedef struct pa_pool pa_pool;
 
 /*
@@ -73,6 +85,7 @@ typedef struct pa_pool_config {
     int32_t max_context_len;   /* largest context length (sizes the split workspace) */
     void *k_cache;             /* device pointer to a caller-owned K pool, or NULL to allocate */
     void *v_cache;             /* same for V */
+    int32_t kv_format;         /* pa_kv_format (0 = 16-bit in the model dtype) */
 } pa_pool_config;
 
 /*
@@ -86,13 +99,15 @@ pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out);
 /* Release everything the pool allocated (not caller-owned caches). NULL is a no-op. */
 void pa_destroy(pa_pool *pool);
 
-/* The pool's own K and V caches (device pointers; the ones passed in or allocated) and their bytes each. */
+/* The pool's own K and V caches (device pointers; the ones passed in or allocated) and their bytes each
+   (for FP8 pools: codes plus scales). */
 pa_status pa_pool_caches(const pa_pool *pool, void **k_cache, void **v_cache, uint64_t *bytes_each);
 
 /*
  * Cache write (scatter): for each token i with slot s = slot_mapping[i] >= 0
  * and each KV head h, copy k[i][h][:] to K[s / block_size][h][s % block_size][:]
- * and v likewise. Raw 16-bit words are copied without conversion; negative
+ * and v likewise. Raw 16-bit words are copied without conversion (FP8 pools:
+ * each row is quantised with its own scale, see pa_kv_format); negative
  * slots are skipped (padding). Slots beyond the pool are skipped and flagged
  * (PA_ERR_DEVICE_BOUNDS). Two tokens with one slot: which one lands is unspecified.
  * (A sequence growing past a block boundary receives a new physical block:

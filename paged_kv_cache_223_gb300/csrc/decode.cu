@@ -34,40 +34,85 @@
 
 namespace pa {
 
-constexpr int STAGES = 3;
+// Pipeline depth per warp and resident CTAs per SM: 16-bit stages are 8 KB (3 stages, 2 CTAs per
+// SM); FP8 stages are 4 KB, so 2 stages leave room for 4 single-column-tile CTAs per SM (16 warps)
+// to hide the per-tile conversion latency.
+#ifndef PA_FP8_STAGES
+#define PA_FP8_STAGES 2
+#endif
+__host__ __device__ constexpr int stages_for(bool kv8) { return kv8 ? PA_FP8_STAGES : 3; }
+__host__ __device__ constexpr int min_ctas_for(bool kv8, int nt) { return kv8 && nt == 1 && PA_FP8_STAGES == 2 ? 4 : 2; }
 
-__host__ __device__ constexpr int ring_bytes(int D) { return DECODE_WARPS * STAGES * 2 * TILE_TOKENS * D * 2; }
+// Shared memory of the tile pipelines. 16-bit pools: each stage holds the K tile then the V tile
+// (16 rows x D 16-bit values each). FP8 pools (D = 128): each stage holds the K codes tile and the V
+// codes tile (16 rows x 128 bytes each, 1024-byte aligned for the 128-byte swizzle); the stages'
+// K and V scales (16 floats each) sit in a small region after all code tiles; then each warp owns
+// one 16-bit tile that it converts K codes into for the scores and then V codes into for P.V.
+__host__ __device__ constexpr int stage_bytes(int D, bool kv8) { return kv8 ? 2 * TILE_TOKENS * 128 : 2 * TILE_TOKENS * D * 2; }
+__host__ __device__ constexpr int scale_region(bool kv8) { return kv8 ? DECODE_WARPS * stages_for(kv8) * 2 * TILE_TOKENS * 4 : 0; }
+__host__ __device__ constexpr int ring_bytes(int D, bool kv8) {
+    return DECODE_WARPS * stages_for(kv8) * stage_bytes(D, kv8) +
+           (kv8 ? ((scale_region(kv8) + 1023) & ~1023) + DECODE_WARPS * TILE_TOKENS * D * 2 : 0);
+}
 __host__ __device__ constexpr int merge_bytes(int D, int nt) {
     return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4;
 }
-__host__ __device__ constexpr int body_bytes(int D, int nt) {
-    return ring_bytes(D) > merge_bytes(D, nt) ? ring_bytes(D) : merge_bytes(D, nt);
+__host__ __device__ constexpr int body_bytes(int D, int nt, bool kv8) {
+    return ring_bytes(D, kv8) > merge_bytes(D, nt) ? ring_bytes(D, kv8) : merge_bytes(D, nt);
 }
 
-static size_t smem_bytes(int D, int nt, int table_entries) {
-    return 1024 /* alignment slack */ + (size_t)body_bytes(D, nt) + DECODE_WARPS * STAGES * 8 +
+static size_t smem_bytes(int D, int nt, bool kv8, int table_entries) {
+    return 1024 /* alignment slack */ + (size_t)body_bytes(D, nt, kv8) + DECODE_WARPS * stages_for(kv8) * 8 +
            (size_t)table_entries * 4;
 }
 
-size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt, 0); }
+size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt, false, 0); }
 
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
+// E4M3 codes of one 16 x 128 tile (128-byte rows, 128-byte swizzle) -> the fp16 tile layout of a
+// 16-bit stage (two 64-value halves of 16 x 128 bytes, same swizzle). Lane l converts row l/2,
+// half l%2; codes are exact in fp16.
+__device__ __forceinline__ void convert_codes(const uint8_t *codes, uint8_t *tile, int lane) {
+    const int r = lane >> 1, h = lane & 1;
+    const uint8_t *src = codes + r * 128;
+    uint8_t *dst = tile + h * (TILE_TOKENS * 128) + r * 128;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;                                   // 16-code chunk: dims 16c..16c+15
+        const uint4 raw = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
+        const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t outw[8];
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) outw[q2] = e4m3x2_to<__half>((uint16_t)(wds[q2 >> 1] >> ((q2 & 1) * 16)));
+        const int c16 = 2 * cc;                                     // 8-value chunks within the half
+        *reinterpret_cast<uint4 *>(dst + ((c16 ^ (r & 7)) << 4)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        *reinterpret_cast<uint4 *>(dst + (((c16 + 1) ^ (r & 7)) << 4)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    }
+}
+
+template <typename T, int D, int NT, bool KV8>
+__global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
+    static_assert(!KV8 || D == 128, "FP8 pools are built for head_dim 128");
+    // FP8 pools compute in fp16 whatever the model dtype: E4M3 codes are exact in fp16 (one cvt per
+    // pair), bf16 queries are exact in fp16 within its normal range, and P times the V scale keeps
+    // fp16's 11 bits. Outputs are rounded to T.
+    using M = typename std::conditional<KV8, __half, T>::type;
     constexpr int HALVES = D / 64;                     // 128-byte swizzle spans per key row
     constexpr int HALF_BYTES = TILE_TOKENS * 128;      // one span of a 16-row tile
-    constexpr int TILE_BYTES = TILE_TOKENS * D * 2;    // K (or V) of one tile
-    constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    constexpr int TILE_BYTES = TILE_TOKENS * D * 2;    // K (or V) of one 16-bit tile
+    constexpr int STAGE_BYTES = stage_bytes(D, KV8);
+    constexpr int CODE_BYTES = TILE_TOKENS * 128;      // FP8: K (or V) codes of one tile
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;                         // m16 tiles of the head dimension (P.V)
+    constexpr int STAGES = stages_for(KV8);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
-    const uint32_t bars_u32 = base_u32 + body_bytes(D, NT);
-    int *tbl = reinterpret_cast<int *>(smem + body_bytes(D, NT) + DECODE_WARPS * STAGES * 8);
+    const uint32_t bars_u32 = base_u32 + body_bytes(D, NT, KV8);
+    int *tbl = reinterpret_cast<int *>(smem + body_bytes(D, NT, KV8) + DECODE_WARPS * STAGES * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -108,6 +153,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
 
     const int my_tiles = ntiles > warp ? (ntiles - warp + DECODE_WARPS - 1) / DECODE_WARPS : 0;
     const uint32_t ring_u32 = base_u32 + warp * STAGES * STAGE_BYTES;
+    const uint32_t scales_u32 = base_u32 + DECODE_WARPS * STAGES * STAGE_BYTES;                 // FP8 only
+    const uint32_t conv_u32 = scales_u32 + ((scale_region(KV8) + 1023) & ~1023) + warp * TILE_BYTES;   // FP8 only
     const uint64_t policy = l2_policy_evict_first();
 
     auto issue = [&](int it) {
@@ -118,11 +165,20 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
         const uint32_t bar = bars_u32 + (warp * STAGES + s) * 8;
         const uint32_t kdst = ring_u32 + s * STAGE_BYTES;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        if constexpr (KV8) {
+            const uint32_t sdst = scales_u32 + (warp * STAGES + s) * 2 * TILE_TOKENS * 4;
+            mbar_arrive_expect_tx(bar, 2 * CODE_BYTES + 2 * TILE_TOKENS * 4);
+            tma_load_2d(kdst, &tmk, 0, row0, bar, policy);
+            tma_load_2d(kdst + CODE_BYTES, &tmv, 0, row0, bar, policy);
+            bulk_load(sdst, p.k_scales + row0, TILE_TOKENS * 4, bar, policy);
+            bulk_load(sdst + TILE_TOKENS * 4, p.v_scales + row0, TILE_TOKENS * 4, bar, policy);
+        } else {
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
 #pragma unroll
-        for (int h = 0; h < HALVES; ++h) {
-            tma_load_2d(kdst + h * HALF_BYTES, &tmk, h * 64, row0, bar, policy);
-            tma_load_2d(kdst + TILE_BYTES + h * HALF_BYTES, &tmv, h * 64, row0, bar, policy);
+            for (int h = 0; h < HALVES; ++h) {
+                tma_load_2d(kdst + h * HALF_BYTES, &tmk, h * 64, row0, bar, policy);
+                tma_load_2d(kdst + TILE_BYTES + h * HALF_BYTES, &tmv, h * 64, row0, bar, policy);
+            }
         }
     };
 
@@ -148,6 +204,14 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
             for (int ks = 0; ks < KSTEPS; ++ks) {
                 qf[nt][ks][0] = __ldg(qrow + ks * 8 + tq);
                 qf[nt][ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
+                if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const __nv_bfloat162 bq = *reinterpret_cast<const __nv_bfloat162 *>(&qf[nt][ks][e]);
+                        const float2 f = __bfloat1622float2(bq);
+                        qf[nt][ks][e] = pack2<__half>(f.x, f.y);
+                    }
+                }
             }
         } else {
 #pragma unroll
@@ -185,13 +249,31 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
         }
         const int i = warp + it * DECODE_WARPS;
         const int tile_t0 = t_begin + i * TILE_TOKENS;   // absolute token index of the tile's first row
-        const uint32_t kb = ring_u32 + s * STAGE_BYTES;
-        const uint32_t vb = kb + TILE_BYTES;
+        const int gq_ = lane >> 2;
+        uint32_t kb = ring_u32 + s * STAGE_BYTES;
+        uint32_t vb = kb + TILE_BYTES;
+        float ks_lo = 1.f, ks_hi = 1.f, vs_lo = 1.f, vs_hi = 1.f;   // FP8: scales of this thread's key rows
+        if constexpr (KV8) {
+            // Convert the tile's K codes into this warp's fp16 tile (same swizzled layout as a 16-bit
+            // stage; codes are exact in fp16). The K scale multiplies the scores and the V scale
+            // multiplies P; the V codes are converted into the same tile after the scores.
+            const float *sk = reinterpret_cast<const float *>(smem + (scales_u32 - base_u32)) +
+                              (warp * STAGES + s) * 2 * TILE_TOKENS;
+            const float *sv = sk + TILE_TOKENS;
+            convert_codes(smem + (kb - base_u32), smem + (conv_u32 - base_u32), lane);
+            ks_lo = sk[gq_] * p.scale_log2;
+            ks_hi = sk[gq_ + 8] * p.scale_log2;
+            vs_lo = sv[gq_];
+            vs_hi = sv[gq_ + 8];
+            __syncwarp();
+            vb = kb + CODE_BYTES;                         // V codes stay in the stage until converted
+            kb = conv_u32;
+        }
 
         // Rows past the context hold other data (possibly NaN): zero them in V so that
         // 0-weight x row stays 0 in the P.V product. Scores of those rows are masked below.
         const int nvalid = L - tile_t0;
-        if (nvalid < TILE_TOKENS) {
+        if (!KV8 && nvalid < TILE_TOKENS) {
             const int nz = (TILE_TOKENS - nvalid) * 8;   // 16-byte chunks per span
             uint8_t *vgen = smem + (vb - base_u32);
             for (int c = lane; c < nz * HALVES; c += 32) {
@@ -215,7 +297,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_16816<T>(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+                for (int nt = 0; nt < NT; ++nt) mma_16816<M>(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
             }
         }
 
@@ -225,8 +307,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const float s0 = t_lo <= lim[nt][j] ? sacc[nt][j] * p.scale_log2 : -INFINITY;
-                const float s1 = t_hi <= lim[nt][j] ? sacc[nt][2 + j] * p.scale_log2 : -INFINITY;
+                const float s0 = t_lo <= lim[nt][j] ? sacc[nt][j] * (KV8 ? ks_lo : p.scale_log2) : -INFINITY;
+                const float s1 = t_hi <= lim[nt][j] ? sacc[nt][2 + j] * (KV8 ? ks_hi : p.scale_log2) : -INFINITY;
                 float mx = fmaxf(s0, s1);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -237,8 +319,14 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                 const float p0 = exp2f(s0 - muse), p1 = exp2f(s1 - muse);
                 l[nt][j] = l[nt][j] * alpha + p0 + p1;
                 m[nt][j] = mnew;
-                sacc[nt][j] = p0;
-                sacc[nt][2 + j] = p1;
+                if constexpr (KV8) {
+                    // V scale of each key row; rows past the context have no scale (select, not multiply)
+                    sacc[nt][j] = t_lo < L ? p0 * vs_lo : 0.f;
+                    sacc[nt][2 + j] = t_hi < L ? p1 * vs_hi : 0.f;
+                } else {
+                    sacc[nt][j] = p0;
+                    sacc[nt][2 + j] = p1;
+                }
 #pragma unroll
                 for (int md = 0; md < MT; ++md) {
                     o[md][nt][j] *= alpha;
@@ -250,7 +338,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
         // The MMA takes P in V's 16-bit type. bf16 keeps 8 mantissa bits, too few for short
         // contexts whose weighted values cancel, so for bf16 P is carried as hi + lo bf16 parts
         // (hi = bf16(P), lo = bf16(P - hi)) and P.V is two MMAs; fp16's 11 bits suffice alone.
-        constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
+        constexpr bool SPLIT_P = std::is_same<M, __nv_bfloat16>::value;
         uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -261,15 +349,36 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                     hi[e] = __bfloat162float(__float2bfloat16_rn(sacc[nt][e]));
                     lo[e] = sacc[nt][e] - hi[e];
                 }
-                pb[nt][0] = movmatrix_trans(pack2<T>(hi[0], hi[1]));
-                pb[nt][1] = movmatrix_trans(pack2<T>(hi[2], hi[3]));
-                pl[nt][0] = movmatrix_trans(pack2<T>(lo[0], lo[1]));
-                pl[nt][1] = movmatrix_trans(pack2<T>(lo[2], lo[3]));
+                pb[nt][0] = movmatrix_trans(pack2<M>(hi[0], hi[1]));
+                pb[nt][1] = movmatrix_trans(pack2<M>(hi[2], hi[3]));
+                pl[nt][0] = movmatrix_trans(pack2<M>(lo[0], lo[1]));
+                pl[nt][1] = movmatrix_trans(pack2<M>(lo[2], lo[3]));
             } else {
-                pb[nt][0] = movmatrix_trans(pack2<T>(sacc[nt][0], sacc[nt][1]));
-                pb[nt][1] = movmatrix_trans(pack2<T>(sacc[nt][2], sacc[nt][3]));
+                pb[nt][0] = movmatrix_trans(pack2<M>(sacc[nt][0], sacc[nt][1]));
+                pb[nt][1] = movmatrix_trans(pack2<M>(sacc[nt][2], sacc[nt][3]));
                 pl[nt][0] = pl[nt][1] = 0u;
             }
+        }
+
+        if constexpr (KV8) {
+            __syncwarp();                                 // every lane's K ldmatrix reads are done
+            convert_codes(smem + (vb - base_u32), smem + (conv_u32 - base_u32), lane);
+            if (nvalid < TILE_TOKENS) {                   // rows past the context: zero (codes may be NaN)
+                const int nz = (TILE_TOKENS - nvalid) * 8;
+                uint8_t *vgen = smem + (conv_u32 - base_u32);
+                for (int c = lane; c < nz * HALVES; c += 32) {
+                    const int h = c / nz, rc = c - (c / nz) * nz;
+                    *reinterpret_cast<uint4 *>(vgen + h * HALF_BYTES + (nvalid + rc / 8) * 128 + (rc % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            __syncwarp();
+            // the stage's codes and scales are consumed: refill it now
+            if (it + STAGES < my_tiles) {
+                if (lane == 0) issue(it + STAGES);
+                ++issued;
+            }
+            vb = conv_u32;
         }
 
         // O^T += V^T . P^T
@@ -283,15 +392,17 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 2)
                 ldsm_x4_trans(addr, a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_16816<T>(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-                    if constexpr (SPLIT_P) mma_16816<T>(o[md][nt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+                    mma_16816<M>(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                    if constexpr (SPLIT_P) mma_16816<M>(o[md][nt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
                 }
             }
         }
         __syncwarp();
-        if (it + STAGES < my_tiles) {
-            if (lane == 0) issue(it + STAGES);
-            ++issued;
+        if constexpr (!KV8) {
+            if (it + STAGES < my_tiles) {
+                if (lane == 0) issue(it + STAGES);
+                ++issued;
+            }
         }
     }
 
@@ -389,7 +500,17 @@ constexpr int MERGE_THREADS = 512;
 // float4 group sums. Each region starts on a 16-byte boundary.
 __host__ __device__ inline int merge_wt_floats(int G, int max_parts) { return (G * max_parts + 3) & ~3; }
 __host__ __device__ inline int merge_den_floats(int G) { return (G + 3) & ~3; }
-__host__ __device__ inline int merge_groups(int pairs) { return MERGE_THREADS / pairs > 0 ? MERGE_THREADS / pairs : 1; }
+// Thread groups per (row, 4 dims) pair: about 8 partitions per thread, at most MERGE_THREADS threads.
+__host__ __device__ inline int merge_groups(int pairs, int max_parts) {
+    int g = (max_parts + 7) / 8;
+    const int cap = MERGE_THREADS / pairs > 0 ? MERGE_THREADS / pairs : 1;
+    return g < 1 ? 1 : (g > cap ? cap : g);
+}
+__host__ __device__ inline int merge_threads(int pairs, int max_parts) {
+    int t = pairs * merge_groups(pairs, max_parts);
+    t = t > MERGE_THREADS ? MERGE_THREADS : t;
+    return (t + 31) & ~31;
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams p) {
@@ -409,7 +530,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row0 = (int64_t)bq * p.Hq + g * G;   // first output row of the unit
 
-    for (int r = warp; r < G; r += MERGE_THREADS / 32) {
+    const int nthreads = blockDim.x;
+    for (int r = warp; r < G; r += nthreads / 32) {
         const float2 *ml = p.part_ml + (row0 + r) * p.max_parts;
         float M = -INFINITY;
         for (int pp = lane; pp < nparts; pp += 32) {
@@ -433,8 +555,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
     __syncthreads();
 
     const int pairs = G * (D / 4);
-    const int groups = merge_groups(pairs);
-    for (int t = threadIdx.x; t < pairs * groups; t += MERGE_THREADS) {
+    const int groups = merge_groups(pairs, p.max_parts);
+    for (int t = threadIdx.x; t < pairs * groups; t += nthreads) {
         const int pair = t % pairs;
         const int grp = t / pairs;
         const int r = pair / (D / 4);
@@ -454,7 +576,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
         sums[grp * pairs + pair] = acc;
     }
     __syncthreads();
-    for (int q = threadIdx.x; q < pairs; q += MERGE_THREADS) {
+    for (int q = threadIdx.x; q < pairs; q += nthreads) {
         float4 t = sums[q];
         for (int k = 1; k < groups; ++k) {
             const float4 u = sums[k * pairs + q];
@@ -474,38 +596,43 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
 
 // ------------------------------------------------------------------ launchers
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool KV8>
 static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t stream) {
-    const size_t smem = smem_bytes(D, NT, (p.part_tokens + p.bs - 1) / p.bs);
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = smem_bytes(D, NT, KV8, (p.part_tokens + p.bs - 1) / p.bs);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)p.num_seqs * p.Hkv * p.max_parts;
-    decode_kernel<T, D, NT><<<(unsigned)grid, DECODE_WARPS * 32, smem, stream>>>(tmk, tmv, p);
+    decode_kernel<T, D, NT, KV8><<<(unsigned)grid, DECODE_WARPS * 32, smem, stream>>>(tmk, tmv, p);
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool KV8>
 static cudaError_t launch_decode_d(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t stream) {
     switch ((p.rows + 7) / 8) {
-        case 1: return launch_decode_t<T, D, 1>(p, tmk, tmv, stream);
-        case 2: return launch_decode_t<T, D, 2>(p, tmk, tmv, stream);
-        case 3: return launch_decode_t<T, D, 3>(p, tmk, tmv, stream);
-        case 4: return launch_decode_t<T, D, 4>(p, tmk, tmv, stream);
+        case 1: return launch_decode_t<T, D, 1, KV8>(p, tmk, tmv, stream);
+        case 2: return launch_decode_t<T, D, 2, KV8>(p, tmk, tmv, stream);
+        case 3: return launch_decode_t<T, D, 3, KV8>(p, tmk, tmv, stream);
+        case 4: return launch_decode_t<T, D, 4, KV8>(p, tmk, tmv, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
-                          const CUtensorMap &tmv, cudaStream_t stream) {
+                          const CUtensorMap &tmv, cudaStream_t stream, bool kv8) {
+    if (kv8) {
+        if (head_dim != 128) return cudaErrorInvalidValue;
+        if (dtype == PA_FP16) return launch_decode_d<__half, 128, true>(p, tmk, tmv, stream);
+        return launch_decode_d<__nv_bfloat16, 128, true>(p, tmk, tmv, stream);
+    }
     if (dtype == PA_FP16) {
-        if (head_dim == 128) return launch_decode_d<__half, 128>(p, tmk, tmv, stream);
-        if (head_dim == 64) return launch_decode_d<__half, 64>(p, tmk, tmv, stream);
+        if (head_dim == 128) return launch_decode_d<__half, 128, false>(p, tmk, tmv, stream);
+        if (head_dim == 64) return launch_decode_d<__half, 64, false>(p, tmk, tmv, stream);
     } else {
-        if (head_dim == 128) return launch_decode_d<__nv_bfloat16, 128>(p, tmk, tmv, stream);
-        if (head_dim == 64) return launch_decode_d<__nv_bfloat16, 64>(p, tmk, tmv, stream);
+        if (head_dim == 128) return launch_decode_d<__nv_bfloat16, 128, false>(p, tmk, tmv, stream);
+        if (head_dim == 64) return launch_decode_d<__nv_bfloat16, 64, false>(p, tmk, tmv, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -513,17 +640,18 @@ cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const 
 size_t merge_smem_bytes(int G, int max_parts, int head_dim) {
     const int pairs = G * (head_dim / 4);
     return (size_t)(merge_wt_floats(G, max_parts) + merge_den_floats(G)) * sizeof(float) +
-           (size_t)merge_groups(pairs) * pairs * sizeof(float4);
+           (size_t)merge_groups(pairs, max_parts) * pairs * sizeof(float4);
 }
 
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
     const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv;
     const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim);
+    const int threads = merge_threads(p.G * (head_dim / 4), p.max_parts);
     cudaError_t e = cudaSuccess;
 #define PA_MERGE(TT, DD)                                                                                       \
     e = cudaFuncSetAttribute(merge_kernel<TT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (e != cudaSuccess) return e;                                                                            \
-    merge_kernel<TT, DD><<<(unsigned)units, MERGE_THREADS, smem, stream>>>(p);
+    merge_kernel<TT, DD><<<(unsigned)units, threads, smem, stream>>>(p);
     if (dtype == PA_FP16) {
         if (head_dim == 128) { PA_MERGE(__half, 128) } else { PA_MERGE(__half, 64) }
     } else {

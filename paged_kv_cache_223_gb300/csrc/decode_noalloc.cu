@@ -115,6 +115,7 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
     p.out = out;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
+    p.k_scales = p.v_scales = nullptr;
     p.part_o = static_cast<float *>(scratch);
     p.part_ml = reinterpret_cast<float2 *>(static_cast<unsigned char *>(scratch) + o_bytes);
     p.status = nullptr;   // no status word on this path: bad ids / lengths are still clamped, not reported

@@ -72,12 +72,15 @@ pa_status tensor_map(pa_pool *pool, const void *cache, CUtensorMap *out) {
     if (!fn) return PA_ERR_CUDA;
     const pa_pool_config &c = pool->cfg;
     CUtensorMap m;
+    const bool kv8 = c.kv_format == PA_KV_FP8_E4M3;
     cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
-    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)TILE_TOKENS};
+    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * (kv8 ? 1 : 2)};
+    cuuint32_t box[2] = {kv8 ? 128u : 64u, (cuuint32_t)TILE_TOKENS};   // 128-byte-wide boxes either way
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(&m, c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                    const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType ty = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : (c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUresult r = fn(&m, ty, 2, const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
     if (pool->maps.size() > 4096) pool->maps.clear();
@@ -126,6 +129,8 @@ pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out) {
     if (c.block_size != 16 && c.block_size != 32) return PA_ERR_UNSUPPORTED;
     if (c.head_dim != 64 && c.head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (c.dtype != PA_FP16 && c.dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (c.kv_format != PA_KV_16BIT && c.kv_format != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if (c.kv_format == PA_KV_FP8_E4M3 && c.head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (c.partition_tokens == 0) c.partition_tokens = 512;
     if (c.partition_tokens < 0 || c.partition_tokens % c.block_size != 0 || c.partition_tokens > 16384)
         return PA_ERR_INVALID_ARG;
@@ -139,7 +144,7 @@ pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out) {
     pa_pool *p = new pa_pool();
     p->cfg = c;
     p->part_tokens = c.partition_tokens;
-    p->cache_bytes = (uint64_t)rows * c.head_dim * 2;
+    p->cache_bytes = c.kv_format == PA_KV_FP8_E4M3 ? (uint64_t)rows * (c.head_dim + 4) : (uint64_t)rows * c.head_dim * 2;
     if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess) {
         delete p;
         return PA_ERR_CUDA;
@@ -201,6 +206,12 @@ pa_status pa_cache_write(pa_pool *pool, const void *k, const void *v, const int6
     const pa_pool_config &c = pool->cfg;
     DeviceGuard g(c.device);
     if (!g.ok) return PA_ERR_CUDA;
+    if (c.kv_format == PA_KV_FP8_E4M3)
+        return launch_cache_write_fp8(k, v, slot_mapping, num_tokens, c.num_kv_heads, c.block_size, c.num_blocks,
+                                      c.dtype, static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache),
+                                      pool->status, pool->sm_count, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? PA_OK
+                   : PA_ERR_CUDA;
     CacheWriteParams p;
     p.k = static_cast<const uint4 *>(k);
     p.v = static_cast<const uint4 *>(v);
@@ -278,13 +289,18 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.scale_log2 = scale * 1.4426950408889634f;
+    const bool kv8 = pool->cfg.kv_format == PA_KV_FP8_E4M3;
+    const int64_t code_bytes = (int64_t)pool->cfg.num_blocks * pool->cfg.num_kv_heads * pool->cfg.block_size *
+                               pool->cfg.head_dim;
+    p.k_scales = kv8 ? reinterpret_cast<const float *>(static_cast<const uint8_t *>(k_cache) + code_bytes) : nullptr;
+    p.v_scales = kv8 ? reinterpret_cast<const float *>(static_cast<const uint8_t *>(v_cache) + code_bytes) : nullptr;
     DeviceGuard g(pool->cfg.device);
     if (!g.ok) return PA_ERR_CUDA;
     CUtensorMap tmk, tmv;
     if ((st = tensor_map(pool, k_cache, &tmk)) != PA_OK) return st;
     if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s, kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
@@ -303,9 +319,23 @@ pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k
     const pa_pool_config &c = pool->cfg;
     DeviceGuard g(c.device);
     if (!g.ok) return PA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (c.kv_format == PA_KV_FP8_E4M3) {
+        // codes of a block, then its scales in the scale region
+        const int64_t code_vec = (int64_t)c.num_kv_heads * c.block_size * c.head_dim / 16;
+        const int64_t scale_vec = (int64_t)c.num_kv_heads * c.block_size * 4 / 16;
+        const int64_t code_bytes = (int64_t)c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim;
+        uint8_t *kc = static_cast<uint8_t *>(k_cache), *vc = static_cast<uint8_t *>(v_cache);
+        if (launch_copy_blocks(pairs, n, kc, vc, code_vec, c.num_blocks, pool->status, pool->sm_count, s) !=
+                cudaSuccess ||
+            launch_copy_blocks(pairs, n, kc + code_bytes, vc + code_bytes, scale_vec, c.num_blocks, pool->status,
+                               pool->sm_count, s) != cudaSuccess)
+            return PA_ERR_CUDA;
+        return PA_OK;
+    }
     const int64_t vec_per_block = (int64_t)c.num_kv_heads * c.block_size * c.head_dim / 8;
     return launch_copy_blocks(pairs, n, k_cache, v_cache, vec_per_block, c.num_blocks, pool->status, pool->sm_count,
-                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+                              s) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }

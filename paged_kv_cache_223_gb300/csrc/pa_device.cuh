@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
@@ -72,6 +73,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -151,6 +162,24 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Two E4M3 codes (first in the low byte) -> two 16-bit values (first in the low half), exactly.
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint16_t codes);
+
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint16_t codes) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint16_t codes) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3);
+    __half2 hh = *reinterpret_cast<__half2 *>(&h);
+    const float2 f = __half22float2(hh);
+    return pack2<__nv_bfloat16>(f.x, f.y);
 }
 
 __device__ __forceinline__ void set_status(int *status, int bit) {

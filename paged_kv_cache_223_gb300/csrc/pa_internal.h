@@ -22,6 +22,8 @@ struct DecodeParams {
     void *out;
     const int32_t *block_tables;
     const int32_t *context_lens;
+    const float *k_scales;  // FP8 pools: per (slot, head) scales of K and V, [num_blocks, Hkv, bs]
+    const float *v_scales;
     float *part_o;       // [num_seqs, q_len, Hq, max_parts, D] unnormalised partition outputs
     float2 *part_ml;     // [num_seqs, q_len, Hq, max_parts] (running max in log2 units, sum)
     int *status;
@@ -57,8 +59,12 @@ struct CacheWriteParams {
 
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_cache_write(const CacheWriteParams &p, int sm_count, cudaStream_t stream);
+// FP8 pools: k, v hold 16-bit rows of the model dtype; caches are codes followed by scales.
+cudaError_t launch_cache_write_fp8(const void *k, const void *v, const int64_t *slots, int64_t num_tokens, int Hkv,
+                                   int bs, int64_t num_blocks, int dtype, uint8_t *k_cache, uint8_t *v_cache,
+                                   int *status, int sm_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
-                          const CUtensorMap &tmv, cudaStream_t stream);
+                          const CUtensorMap &tmv, cudaStream_t stream, bool kv8 = false);
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OOM, PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT = range(7)
 PA_FP16, PA_BF16 = 0, 1
+PA_KV_16BIT, PA_KV_FP8_E4M3 = 0, 1
 _TORCH_DTYPE = {PA_FP16: torch.float16, PA_BF16: torch.bfloat16}
 _PA_DTYPE = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
 
@@ -27,7 +28,7 @@ class PaPoolConfig(C.Structure):
                 ("head_dim", C.c_int32), ("dtype", C.c_int32), ("device", C.c_int32),
                 ("partition_tokens", C.c_int32), ("max_seqs", C.c_int32), ("max_q_heads", C.c_int32),
                 ("max_q_len", C.c_int32), ("max_context_len", C.c_int32), ("k_cache", C.c_void_p),
-                ("v_cache", C.c_void_p)]
+                ("v_cache", C.c_void_p), ("kv_format", C.c_int32)]
 
 
 class PagedAttnError(RuntimeError):
@@ -97,28 +98,36 @@ def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> tor
 class Pool:
     """One paged KV pool (pa_pool_create) with its caches.
 
-    The caches are torch tensors [num_blocks, num_kv_heads, block_size, head_dim], created
-    here unless given; the pool only borrows them.
+    The caches are torch tensors, created here unless given; the pool only borrows them.
+    16-bit pools: [num_blocks, num_kv_heads, block_size, head_dim] of the model dtype.
+    FP8 pools (kv_format=PA_KV_FP8_E4M3): one uint8 buffer each of num_blocks*Hkv*bs*(head_dim + 4)
+    bytes (codes, then float32 scales).
     """
 
     def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                  dtype: torch.dtype = torch.float16, device: int = 0, partition_tokens: int = 0,
                  max_seqs: int = 256, max_q_heads: int = 64, max_q_len: int = 8, max_context_len: int = 8192,
-                 k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None):
+                 k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
+                 kv_format: int = PA_KV_16BIT):
         self.geometry = (num_blocks, num_kv_heads, block_size, head_dim)
         self.dtype = dtype
+        self.kv_format = kv_format
         self.device = torch.device("cuda", device)
+        if kv_format == PA_KV_FP8_E4M3:
+            shape, cdt = (num_blocks * num_kv_heads * block_size * (head_dim + 4),), torch.uint8
+        else:
+            shape, cdt = self.geometry, dtype
         if k_cache is None:
-            k_cache = torch.empty(self.geometry, dtype=dtype, device=self.device)
-            v_cache = torch.empty(self.geometry, dtype=dtype, device=self.device)
+            k_cache = torch.empty(shape, dtype=cdt, device=self.device)
+            v_cache = torch.empty(shape, dtype=cdt, device=self.device)
         for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
-            _dev(t, name, dtype)
-            if tuple(t.shape) != self.geometry:
-                raise ValueError(f"{name} must have shape {self.geometry}")
+            _dev(t, name, cdt)
+            if tuple(t.shape) != tuple(shape):
+                raise ValueError(f"{name} must have shape {tuple(shape)}")
         self.k_cache, self.v_cache = k_cache, v_cache
         cfg = PaPoolConfig(num_blocks, block_size, num_kv_heads, head_dim, _PA_DTYPE[dtype], device,
                            partition_tokens, max_seqs, max_q_heads, max_q_len, max_context_len,
-                           k_cache.data_ptr(), v_cache.data_ptr())
+                           k_cache.data_ptr(), v_cache.data_ptr(), kv_format)
         h = C.c_void_p()
         _check(lib().pa_pool_create(C.byref(cfg), C.byref(h)), "pa_pool_create")
         self._h = h

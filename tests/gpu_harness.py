@@ -23,14 +23,27 @@ DEV = torch.device("cuda", 0)
 
 
 def make_pool(wl: synth.Workload, partition_tokens: int = 0, k_cache=None, v_cache=None,
-              max_context_len: Optional[int] = None) -> pa.Pool:
+              max_context_len: Optional[int] = None, kv_format: int = pa.PA_KV_16BIT) -> pa.Pool:
     return pa.Pool(wl.num_blocks, wl.bs, wl.Hkv, wl.d, TORCH_DT[wl.dtype], 0,
                    partition_tokens=partition_tokens or wl.partition_tokens, max_seqs=wl.B, max_q_heads=wl.Hq,
                    max_q_len=wl.q_len, max_context_len=max_context_len or wl.stride * wl.bs,
-                   k_cache=k_cache, v_cache=v_cache)
+                   k_cache=k_cache, v_cache=v_cache, kv_format=kv_format)
 
 
-def alloc_caches(wl: synth.Workload) -> Tuple[torch.Tensor, torch.Tensor]:
+FP8_NAN_CODE = 0x7F
+
+
+def alloc_caches(wl: synth.Workload, kv_format: int = pa.PA_KV_16BIT) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Caches filled with NaN sentinels (16-bit: the NaN word; FP8: the NaN code and NaN scales)."""
+    if kv_format == pa.PA_KV_FP8_E4M3:
+        codes = wl.num_blocks * wl.Hkv * wl.bs * wl.d
+        out = []
+        for _ in range(2):
+            buf = torch.empty(codes + 4 * wl.num_blocks * wl.Hkv * wl.bs, dtype=torch.uint8, device=DEV)
+            buf[:codes].fill_(FP8_NAN_CODE)
+            buf[codes:].view(torch.int32).fill_(0x7FC00000)
+            out.append(buf)
+        return out[0], out[1]
     shape = (wl.num_blocks, wl.Hkv, wl.bs, wl.d)
     kc = torch.empty(shape, dtype=TORCH_DT[wl.dtype], device=DEV)
     vc = torch.empty_like(kc)
@@ -62,10 +75,10 @@ def device_inputs(wl: synth.Workload, layer: int):
     return q, tables, lens
 
 
-def build_device(wl: synth.Workload, layer: int = 0, partition_tokens: int = 0):
+def build_device(wl: synth.Workload, layer: int = 0, partition_tokens: int = 0, kv_format: int = pa.PA_KV_16BIT):
     """Pool + caches filled through pa_cache_write (fill, then the newest tokens) + q/tables/lens."""
-    kc, vc = alloc_caches(wl)
-    pool = make_pool(wl, partition_tokens, kc, vc)
+    kc, vc = alloc_caches(wl, kv_format)
+    pool = make_pool(wl, partition_tokens, kc, vc, kv_format=kv_format)
     fill(pool, wl, layer, kc, vc, new_only=False)
     fill(pool, wl, layer, kc, vc, new_only=True)
     q, tables, lens = device_inputs(wl, layer)
@@ -133,3 +146,35 @@ def check_pool_blocks(wl: synth.Workload, layer: int, kc, vc, hk, hv, seqs: Sequ
             exp_t = exp.transpose(0, 2, 1, 3).reshape(nb * wl.bs, wl.Hkv, wl.d)
             assert np.array_equal(got_t[:L], exp_t[:L]), f"seq {b}: cache words differ"
             assert (got_t[L:] == nanw).all(), f"seq {b}: slots past the context were written"
+
+
+def oracle_reference_fp8(wl: synth.Workload, layer: int, seqs: Optional[Sequence[int]] = None):
+    """The oracle's FP8 chain (quantising cache write -> gather -> dequantise -> attention) for `seqs`.
+    Returns (out float64, host K buffer, host V buffer) in the pool's FP8 layout."""
+    wl = synth.with_layer(wl, layer)
+    seqs = list(range(wl.B)) if seqs is None else list(seqs)
+    geo = (wl.num_blocks, wl.Hkv, wl.bs, wl.d)
+    hk = oracle.fp8_pool(*geo)
+    hv = oracle.fp8_pool(*geo)
+    for b in seqs:
+        t = np.arange(int(wl.context_lens[b]), dtype=np.int64)
+        oracle.cache_write_fp8(hk, hv, geo, wl.kv_values(layer, b, t, "k"), wl.kv_values(layer, b, t, "v"),
+                               wl.slots(b, t), wl.dtype)
+    q = wl.q_values(layer, np.array(seqs))
+    out = oracle.paged_attention_fp8(q, hk, hv, geo, wl.block_tables, wl.context_lens, wl.dtype, wl.scale,
+                                     seqs=np.array(seqs))
+    return out, hk, hv
+
+
+def check_fp8_pool_rows(wl: synth.Workload, layer: int, kc, vc, hk, hv, seqs: Sequence[int]):
+    """Codes and scales of the listed sequences' valid slots equal the oracle's, bit for bit."""
+    wl = synth.with_layer(wl, layer)
+    geo = (wl.num_blocks, wl.Hkv, wl.bs, wl.d)
+    for dev_buf, host_buf in ((kc, hk), (vc, hv)):
+        dc, ds = oracle.fp8_views(dev_buf.cpu().numpy(), *geo)
+        hc, hs = oracle.fp8_views(host_buf, *geo)
+        for b in seqs:
+            t = np.arange(int(wl.context_lens[b]))
+            pb, off = wl.block_tables[b, t // wl.bs], t % wl.bs
+            assert np.array_equal(dc[pb, :, off], hc[pb, :, off]), f"seq {b}: codes differ"
+            assert np.array_equal(ds[pb, :, off].view(np.uint32), hs[pb, :, off].view(np.uint32)), f"seq {b}: scales"

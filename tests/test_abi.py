@@ -46,9 +46,11 @@ def test_status_strings(lib):
 
 def test_host_validation_without_gpu(lib):
     good = dict(num_blocks=64, block_size=16, num_kv_heads=2, head_dim=64, dtype=0, device=0, partition_tokens=0,
-                max_seqs=4, max_q_heads=8, max_q_len=1, max_context_len=256, k_cache=None, v_cache=None)
+                max_seqs=4, max_q_heads=8, max_q_len=1, max_context_len=256, k_cache=None, v_cache=None,
+                kv_format=0)
     bad = [dict(block_size=8), dict(head_dim=96), dict(num_blocks=0), dict(dtype=5), dict(partition_tokens=24),
-           dict(max_q_len=9), dict(k_cache=16), dict(max_seqs=0), dict(device=-1)]
+           dict(max_q_len=9), dict(k_cache=16), dict(max_seqs=0), dict(device=-1), dict(kv_format=3),
+           dict(kv_format=1, head_dim=64)]
     for b in bad:
         st = lib.pool_create_status(**{**good, **b})
         assert st in (lib.PA_ERR_INVALID_ARG, lib.PA_ERR_UNSUPPORTED), b
