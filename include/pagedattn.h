@@ -154,6 +154,32 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
                     void *stream);
 
 /*
+ * Chunked prefill: attention for a chunk of q_len new tokens per sequence, the
+ * chunk's K and V already written to the pool (pa_cache_write). A long prompt
+ * is processed in chunks (yangyu.win blog #54, section 4 "Chunked Prefill":
+ * an 8,000-token prompt as 512-token chunks); chunk row qi sits at position
+ * context_lens[b] - q_len + qi and attends causally to tokens 0..that position,
+ * which is exactly pa_decode's definition with a large q_len (learn.tanhdev.com
+ * part 8: A_i = softmax(q_i K^T / sqrt(d_k)), o_i = sum a v). The products run
+ * on the 5th-generation tensor cores (tcgen05.mma, fp32 accumulators in tensor
+ * memory); the softmax is fp32; out is rounded to nearest even.
+ * Requires a 16-bit pool with head_dim 128 (PA_ERR_UNSUPPORTED otherwise).
+ * Uses no workspace: concurrent calls on one pool are allowed.
+ *   q              device [num_seqs, q_len, num_q_heads, 128]
+ *   k_cache, v_cache  device pools, or NULL for the pool's own
+ *   block_tables   device int32 [num_seqs, block_table_stride]
+ *   context_lens   device int32 [num_seqs]; q_len <= context_lens[b] <= stride * bs
+ *                  (violations are flagged, PA_ERR_DEVICE_BOUNDS at pa_pool_check)
+ *   q_len          1 .. PA_PREFILL_MAX_Q_LEN; num_q_heads a multiple of num_kv_heads
+ *   out            device [num_seqs, q_len, num_q_heads, 128]
+ */
+#define PA_PREFILL_MAX_Q_LEN 8192
+pa_status pa_prefill(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                     int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale, void *out,
+                     void *stream);
+
+/*
  * Synchronise the device, read and clear the pool's status word.
  * Returns PA_OK, PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT or PA_ERR_CUDA.
  */

@@ -305,6 +305,57 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     return PA_OK;
 }
 
+pa_status pa_prefill(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                     int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale, void *out, void *stream) {
+    if (!pool || !q || !out || !block_tables || !context_lens || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    const pa_pool_config &c = pool->cfg;
+    if (c.kv_format != PA_KV_16BIT || c.head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!k_cache) {
+        k_cache = pool->k_cache;
+        v_cache = pool->v_cache;
+    }
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    if (block_table_stride < 1 || num_seqs < 1 || num_q_heads < 1 || num_q_heads % c.num_kv_heads != 0 || q_len < 1 ||
+        q_len > PA_PREFILL_MAX_Q_LEN)
+        return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / c.num_kv_heads;
+    const int64_t rows = (int64_t)G * q_len;
+    if (rows > ((int64_t)1 << 24) || (int64_t)num_seqs * c.num_kv_heads * ((rows + 127) / 128) >= ((int64_t)1 << 31))
+        return PA_ERR_UNSUPPORTED;
+    int64_t max_ctx = (int64_t)block_table_stride * c.block_size;
+    if (max_ctx > c.max_context_len) max_ctx = c.max_context_len;
+    DecodeParams p = {};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = pool->status;
+    p.stride = block_table_stride;
+    p.num_seqs = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = c.num_kv_heads;
+    p.G = G;
+    p.q_len = q_len;
+    p.rows = (int)rows;
+    p.bs = c.block_size;
+    p.num_blocks = c.num_blocks;
+    p.max_ctx = (int)max_ctx;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_ns = pool->wait_ns;
+    DeviceGuard g(c.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    CUtensorMap tmk, tmv;
+    pa_status st;
+    if ((st = tensor_map(pool, k_cache, &tmk)) != PA_OK) return st;
+    if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
+    return launch_prefill(p, c.dtype, tmk, tmv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                                 : PA_ERR_CUDA;
+}
+
 pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k_cache, void *v_cache,
                          void *stream) {
     if (!pool || n < 0) return PA_ERR_INVALID_ARG;

@@ -72,7 +72,10 @@ cudaError_t launch_spec_verify(const float *p, const float *q, const int32_t *dr
                                cudaStream_t stream);
 cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n, void *k_cache, void *v_cache, int64_t vec_per_block,
                                int32_t num_blocks, int *status, int sm_count, cudaStream_t stream);
+cudaError_t launch_prefill(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int nt);
+size_t prefill_smem_bytes();
 size_t merge_smem_bytes(int G, int max_parts, int head_dim);
 constexpr size_t MAX_SMEM_PER_CTA = 227 * 1024;
 

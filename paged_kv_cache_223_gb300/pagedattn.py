@@ -57,6 +57,7 @@ def lib() -> C.CDLL:
             L.pa_pool_caches.argtypes = [P, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.POINTER(C.c_uint64)]
             L.pa_cache_write.argtypes = [P, P, P, P, I32, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
+            L.pa_prefill.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
             L.pa_pool_check.argtypes = [P, P]
             L.pa_pool_selftest_wait.argtypes = [P, C.c_uint64, P]
             L.pa_pool_selftest_wait.restype = C.c_int
@@ -64,7 +65,7 @@ def lib() -> C.CDLL:
             L.pa_decode_launches.restype = I32
             L.pa_status_string.argtypes = [C.c_int]
             L.pa_status_string.restype = C.c_char_p
-            for f in ("pa_pool_create", "pa_pool_caches", "pa_cache_write", "pa_decode", "pa_pool_check"):
+            for f in ("pa_pool_create", "pa_pool_caches", "pa_cache_write", "pa_decode", "pa_prefill", "pa_pool_check"):
                 getattr(L, f).restype = C.c_int
             _lib = L
     return _lib
@@ -171,6 +172,22 @@ class Pool:
         _check(lib().pa_decode(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
                                _stream(stream)), "pa_decode")
+        return out
+
+    def prefill(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                out: Optional[torch.Tensor] = None, k_cache: Optional[torch.Tensor] = None,
+                v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Chunked prefill (pa_prefill): q [B, C, Hq, 128] is a chunk of C new tokens per sequence, causal."""
+        _dev(q, "q", self.dtype)
+        _dev(block_tables, "block_tables", torch.int32)
+        _dev(context_lens, "context_lens", torch.int32)
+        B, q_len, Hq, d = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        _dev(out, "out", self.dtype)
+        _check(lib().pa_prefill(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
+                                _stream(stream)), "pa_prefill")
         return out
 
     def launches(self, block_table_stride: int, num_seqs: int, num_q_heads: int, q_len: int) -> int:

@@ -26,7 +26,7 @@ def make_pool(wl: synth.Workload, partition_tokens: int = 0, k_cache=None, v_cac
               max_context_len: Optional[int] = None, kv_format: int = pa.PA_KV_16BIT) -> pa.Pool:
     return pa.Pool(wl.num_blocks, wl.bs, wl.Hkv, wl.d, TORCH_DT[wl.dtype], 0,
                    partition_tokens=partition_tokens or wl.partition_tokens, max_seqs=wl.B, max_q_heads=wl.Hq,
-                   max_q_len=wl.q_len, max_context_len=max_context_len or wl.stride * wl.bs,
+                   max_q_len=min(wl.q_len, 8), max_context_len=max_context_len or wl.stride * wl.bs,
                    k_cache=k_cache, v_cache=v_cache, kv_format=kv_format)
 
 

@@ -1,0 +1,90 @@
+"""GPU parity of the chunked prefill (pa_prefill, tcgen05 tensor cores) against the fp64 oracle.
+
+A chunk of C new tokens per sequence is written to the pool through pa_cache_write after the
+earlier tokens; pa_prefill then computes the chunk's causal attention, which the oracle computes
+as paged attention with q_len = C. Outputs element-wise within |gpu - oracle| <= 2e-3 + 1e-2 |oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from paged_kv_cache_223_gb300 import pagedattn as pa
+
+pytestmark = pytest.mark.gpu
+
+import gpu_harness as H  # noqa: E402
+
+CASES = [
+    # (lens, Hq, Hkv, bs, C, dtype, prefix)
+    ([512], 32, 8, 16, 512, synth.FP16, 0),                 # first chunk of a prompt: context == chunk
+    ([1024, 1536], 32, 8, 16, 512, synth.BF16, 0),          # later chunks, G = 4
+    ([77, 300, 1000], 16, 4, 16, 77, synth.FP16, 0),        # ragged contexts, 308 rows: ragged row tile
+    ([200, 1000], 8, 8, 32, 200, synth.BF16, 0),            # MHA (G = 1), bs 32
+    ([100, 450], 24, 8, 16, 100, synth.FP16, 0),            # G = 3: a chunk position spans two row tiles
+    ([1, 300], 8, 2, 16, 1, synth.BF16, 0),                 # C = 1 (a decode step through the prefill path)
+    ([63, 64, 65, 129], 16, 2, 16, 63, synth.FP16, 0),      # contexts at the 64-token tile edges
+    ([1024 + 300, 1024 + 300], 32, 8, 16, 300, synth.BF16, 1024),   # shared copy-on-write prefix
+    ([4096 + 512], 64, 8, 16, 512, synth.BF16, 0),          # 70B-style heads (G = 8), 4096 rows per KV head
+    ([2048 + 7], 16, 1, 32, 7, synth.FP16, 0),              # one KV head (G = 16), short chunk, long context
+]
+
+
+def run_prefill(wl, stress_rows=None):
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    out = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    return pool, kc, vc, out
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"chunk{i}" for i in range(len(CASES))])
+def test_prefill_parity(case):
+    lens, Hq, Hkv, bs, C, dt, pre = case
+    wl = synth.custom_workload(lens, Hq, Hkv, 128, bs, C, dt, prefix_tokens=pre, tag=300 + CASES.index(case))
+    pool, kc, vc, out = run_prefill(wl)
+    ref, hk, hv = H.oracle_reference(wl, 0)
+    H.check_pool_blocks(wl, 0, kc, vc, hk, hv, range(wl.B))
+    H.assert_close(out, ref, f"prefill {case}")
+
+
+@pytest.mark.parametrize("stress", ["qx8", "vmean"])
+def test_prefill_stress(stress):
+    """Peaked softmax (q x 8: the running max moves often and far) and V with mean 1."""
+    kw = dict(q_sigma=8.0) if stress == "qx8" else dict(v_mean=1.0)
+    wl = synth.custom_workload([700, 1300], 32, 8, 128, 16, 256, synth.BF16, tag=320, **kw)
+    _, _, _, out = run_prefill(wl)
+    ref, _, _ = H.oracle_reference(wl, 0)
+    H.assert_close(out, ref, f"prefill {stress}")
+
+
+def test_prefill_matches_decode_for_short_chunks():
+    """For q_len <= 8 both entry points compute the same definition: both within tolerance of the oracle,
+    and close to each other."""
+    wl = synth.custom_workload([40, 700, 2000], 32, 8, 128, 16, 4, synth.FP16, tag=321)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    a = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    b = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _, _ = H.oracle_reference(wl, 0)
+    H.assert_close(a, ref, "prefill")
+    H.assert_close(b, ref, "decode")
+
+
+def test_prefill_deterministic_and_rejects():
+    wl = synth.custom_workload([300, 500], 16, 4, 128, 16, 128, synth.FP16, tag=322)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    a = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    b = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # a context shorter than the chunk is flagged on the device
+    bad = lens.clone()
+    bad[0] = 100
+    pool.prefill(q, tables, bad, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_ERR_DEVICE_BOUNDS
+    # head_dim 64 pools are not supported by the prefill path
+    small = pa.Pool(16, 16, 2, 64, torch.float16, 0, max_seqs=1, max_q_heads=4, max_q_len=1, max_context_len=256)
+    q64 = torch.zeros((1, 4, 4, 64), dtype=torch.float16, device=H.DEV)
+    t = torch.zeros((1, 16), dtype=torch.int32, device=H.DEV)
+    n = torch.full((1,), 4, dtype=torch.int32, device=H.DEV)
+    with pytest.raises(RuntimeError):
+        small.prefill(q64, t, n, 0.125)
