@@ -171,6 +171,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
  *   context_lens   device int32 [num_seqs]; q_len <= context_lens[b] <= stride * bs
  *                  (violations are flagged, PA_ERR_DEVICE_BOUNDS at pa_pool_check)
  *   q_len          1 .. PA_PREFILL_MAX_Q_LEN; num_q_heads a multiple of num_kv_heads
+ *   scale          softmax scale, finite and > 0 (1/sqrt(head_dim) in the pages' formula)
  *   out            device [num_seqs, q_len, num_q_heads, 128]
  */
 #define PA_PREFILL_MAX_Q_LEN 8192

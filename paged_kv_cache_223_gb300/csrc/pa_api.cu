@@ -308,7 +308,8 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
 pa_status pa_prefill(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
                      int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale, void *out, void *stream) {
-    if (!pool || !q || !out || !block_tables || !context_lens || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!pool || !q || !out || !block_tables || !context_lens || !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
     if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
     const pa_pool_config &c = pool->cfg;
     if (c.kv_format != PA_KV_16BIT || c.head_dim != 128) return PA_ERR_UNSUPPORTED;

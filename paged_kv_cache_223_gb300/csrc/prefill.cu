@@ -8,17 +8,19 @@
 // q_len = C (learn.tanhdev.com part 8: A_i = softmax(q_i K^T / sqrt(d_k)), o_i = sum a v).
 //
 // A query "row" is one (chunk position, query head of the KV group) pair: r = qi * G + h. One CTA
-// takes two tiles of 128 rows of one (sequence, KV head) and walks the keys in 64-token tiles, the
-// two row tiles in ping-pong so that one tile's softmax overlaps the other's matrix products:
+// takes two tiles of 128 rows of one (sequence, KV head) and walks the keys in 64-token tiles:
 //   warp 8 (producer)  block-table lookups and TMA copies of K/V tiles into a ring of stages
-//   warp 9 (MMA)       S_t = Q_t K^T  (tcgen05.mma M=128 N=64 K=128, both operands K-major)
-//                      O_t += P_t V   (M=128 N=128 K=64, V as an MN-major operand)
+//   warp 9 (MMA)       S_t = Q_t K^T  (tcgen05.mma M=128 N=64 K=128 from shared memory) -> TMEM
+//                      O_t += P_t V   (M=128 N=128 K=64: P read from TMEM, V an MN-major smem operand)
 //                      one elected thread issues; completion is signalled by tcgen05.commit
 //   warps 0-3, 4-7     softmax of row tile 0 and 1, one row per thread = one tensor-memory lane:
 //                      S from TMEM, causal mask, running max (the O rescale is skipped while the
-//                      max grows by less than 2^8), row sum, P to shared memory (bf16: hi + lo)
-// Per row tile the MMA warp issues P.V of key tile j-1 before S of key tile j, so the commit of
-// S(j) also covers P.V(j-1): the softmax of tile j may rescale O and overwrite P without a wait.
+//                      max grows by less than 2^8), row sum, P (bf16: hi + lo parts) written back to
+//                      TMEM over the S it came from
+// Tensor memory per row tile: two S buffers of 64 columns (S of key tile j in buffer j & 1) and O
+// (128 columns). S of key tile j is issued before P.V of tile j-1, so the softmax of tile j runs
+// while the tensor cores finish tile j-1; MMAs of one thread execute in issue order, so S(j+2)
+// overwrites P(j) only after P(j).V has read it.
 #include "pa_device.cuh"
 
 namespace pa {
@@ -34,20 +36,18 @@ constexpr int PF_THREADS = PF_SM_THREADS + 64;
 constexpr int PF_Q_BYTES = PF_BM * PF_D * 2;                  // 32 KB: 2 halves of [128 rows x 128 B]
 constexpr int PF_KV_BYTES = PF_BN * PF_D * 2;                 // 16 KB: 2 halves of [64 rows x 128 B]
 constexpr int PF_STAGE_BYTES = 2 * PF_KV_BYTES;               // K tile + V tile
-constexpr int PF_P_BYTES = PF_BM * PF_BN * 2;                 // 16 KB: [128 rows x 128 B]
-constexpr uint32_t PF_TMEM_COLS = 512;                        // S_t: 64 t, O_t: 128 + 128 t
+constexpr uint32_t PF_TMEM_COLS = 512;                        // row tile t: S at 256 t (+64), O at 256 t + 128
 constexpr float PF_RESCALE_LOG2 = 8.f;                        // stale-max headroom (P <= 2^8)
 
 template <typename T>
 struct PrefillLayout {
     static constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int STAGES = SPLIT_P ? 3 : 4;
-    static constexpr int P_TILE = (SPLIT_P ? 2 : 1) * PF_P_BYTES;
+    static constexpr int STAGES = 4;
     static constexpr int OFF_STAGE = PF_QT * PF_Q_BYTES;
-    static constexpr int OFF_P = OFF_STAGE + STAGES * PF_STAGE_BYTES;
-    static constexpr int OFF_BAR = OFF_P + PF_QT * P_TILE;
-    // barriers: kv_full[STAGES], kv_empty[STAGES], s_full[2], p_full[2], o_done[2], drain
-    static constexpr int NBAR = 2 * STAGES + 3 * PF_QT + 1;
+    static constexpr int OFF_BAR = OFF_STAGE + STAGES * PF_STAGE_BYTES;
+    // barriers: kv_full[STAGES], kv_empty[STAGES], then per row tile s_full[2], p_full[2], o_bar[2],
+    // then o_done[2], drain
+    static constexpr int NBAR = 2 * STAGES + 6 * PF_QT + PF_QT + 1;
     static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
 };
 static_assert(PrefillLayout<__half>::SMEM <= 227 * 1024, "prefill shared memory");
@@ -68,9 +68,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     uint8_t *smem = smem_raw + (base - raw_u32);
     const uint32_t bar_kv_full = base + LY::OFF_BAR;
     const uint32_t bar_kv_empty = bar_kv_full + STAGES * 8;
-    const uint32_t bar_s_full = bar_kv_empty + STAGES * 8;
-    const uint32_t bar_p_full = bar_s_full + PF_QT * 8;
-    const uint32_t bar_o_done = bar_p_full + PF_QT * 8;
+    const uint32_t bar_s_full = bar_kv_empty + STAGES * 8;        // [t][buffer]
+    const uint32_t bar_p_full = bar_s_full + PF_QT * 16;          // [t][buffer]
+    const uint32_t bar_o_bar = bar_p_full + PF_QT * 16;           // [t][buffer]: P.V of that buffer done
+    const uint32_t bar_o_done = bar_o_bar + PF_QT * 16;
     const uint32_t bar_drain = bar_o_done + PF_QT * 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + LY::OFF_BAR + LY::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mtiles = (p.rows + PF_BM - 1) / PF_BM;
     const int ctiles = (mtiles + PF_QT - 1) / PF_QT;
-    const int ct = blockIdx.x % ctiles;
+    const int ct = ctiles - 1 - (int)(blockIdx.x % ctiles);  // the unit's longest row tiles start first
     const int bg = blockIdx.x / ctiles;
     const int g = bg % p.Hkv, b = bg / p.Hkv;
 
@@ -107,11 +108,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             mbar_init(bar_kv_full + s * 8, 1);
             mbar_init(bar_kv_empty + s * 8, 1);
         }
-        for (int t = 0; t < PF_QT; ++t) {
-            mbar_init(bar_s_full + t * 8, 1);
-            mbar_init(bar_p_full + t * 8, PF_BM);
-            mbar_init(bar_o_done + t * 8, 1);
+        for (int i = 0; i < 2 * PF_QT; ++i) {
+            mbar_init(bar_s_full + i * 8, 1);
+            mbar_init(bar_p_full + i * 8, PF_BM);
+            mbar_init(bar_o_bar + i * 8, 1);
         }
+        for (int t = 0; t < PF_QT; ++t) mbar_init(bar_o_done + t * 8, 1);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         *issued_tiles = 0;
@@ -142,68 +144,74 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
     if (warp == PF_PRODUCER_WARP) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_last();   // re-read by the unit's other row tiles
-            int j = 0;
-            for (; j < ntiles; ++j) {
-                const int st = j % STAGES;
-                if (j >= STAGES &&
-                    !mbar_wait_bounded(bar_kv_empty + st * 8, (uint32_t)((j - STAGES) / STAGES) & 1u, p.wait_ns)) {
-                    *abort_flag = 1;
+        // A tile is 16 copies of 16 rows x 128 bytes (4 sub-tiles x 2 halves x K/V), one per lane:
+        // a single thread issuing them all could not keep the tensor cores fed. Each lane looks up
+        // its sub-tile's block one tile ahead.
+        const uint64_t policy = l2_policy_evict_last();       // re-read by the unit's other row tiles
+        const int sb = lane >> 2, h = (lane >> 1) & 1, is_v = lane & 1;
+        const bool copier = lane < 4 * (PF_BN / TILE_TOKENS);
+        auto lookup = [&](int j) -> int {
+            const int tok = j * PF_BN + sb * TILE_TOKENS;
+            return (copier && tok < L) ? __ldg(p.block_tables + (int64_t)b * p.stride + tok / p.bs) : 0;
+        };
+        int id_next = ntiles > 0 ? lookup(0) : 0;
+        int j = 0;
+        for (; j < ntiles; ++j) {
+            const int st = j % STAGES;
+            if (j >= STAGES) {
+                const bool got =
+                    mbar_wait_bounded(bar_kv_empty + st * 8, (uint32_t)((j - STAGES) / STAGES) & 1u, p.wait_ns);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0) *abort_flag = 1;
                     break;
                 }
-                if (*abort_flag) break;
-                int ids[PF_BN / TILE_TOKENS];
-                int nsub = 0;
-#pragma unroll
-                for (int sb = 0; sb < PF_BN / TILE_TOKENS; ++sb) {
-                    const int tok = j * PF_BN + sb * TILE_TOKENS;
-                    ids[sb] = tok < L ? __ldg(p.block_tables + (int64_t)b * p.stride + tok / p.bs) : 0;
-                    nsub += tok < L;
-                }
-                const uint32_t kdst = base + LY::OFF_STAGE + st * PF_STAGE_BYTES, vdst = kdst + PF_KV_BYTES;
-                const uint32_t bar = bar_kv_full + st * 8;
-                mbar_arrive_expect_tx(bar, nsub * 4 * TILE_TOKENS * 128);
-#pragma unroll
-                for (int sb = 0; sb < PF_BN / TILE_TOKENS; ++sb) {
-                    if (sb < nsub) {
-                        int id = ids[sb];
-                        if (id < 0 || id >= p.num_blocks) {
-                            set_status(p.status, STATUS_BOUNDS);
-                            id = 0;
-                        }
-                        const int tok = j * PF_BN + sb * TILE_TOKENS;
-                        const int row0 = (id * p.Hkv + g) * p.bs + tok % p.bs;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t off = h * (PF_BN * 128) + sb * TILE_TOKENS * 128;
-                            tma_load_2d(kdst + off, &tmk, h * 64, row0, bar, policy);
-                            tma_load_2d(vdst + off, &tmv, h * 64, row0, bar, policy);
-                        }
-                    }
-                }
             }
-            *issued_tiles = j;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            int id = id_next;
+            if (j + 1 < ntiles) id_next = lookup(j + 1);
+            const int rem = L - j * PF_BN;                     // > 0 for every tile issued
+            const int nsub = rem >= PF_BN ? PF_BN / TILE_TOKENS : (rem + TILE_TOKENS - 1) / TILE_TOKENS;
+            const uint32_t bar = bar_kv_full + st * 8;
+            if (lane == 0) mbar_arrive_expect_tx(bar, nsub * 4 * TILE_TOKENS * 128);
+            __syncwarp();
+            if (copier && sb < nsub) {
+                if (id < 0 || id >= p.num_blocks) {
+                    set_status(p.status, STATUS_BOUNDS);
+                    id = 0;
+                }
+                const int tok = j * PF_BN + sb * TILE_TOKENS;
+                const int row0 = (id * p.Hkv + g) * p.bs + tok % p.bs;
+                const uint32_t dst = base + LY::OFF_STAGE + st * PF_STAGE_BYTES + is_v * PF_KV_BYTES +
+                                     h * (PF_BN * 128) + sb * TILE_TOKENS * 128;
+                tma_load_2d(dst, is_v ? &tmv : &tmk, h * 64, row0, bar, policy);
+            }
         }
+        if (lane == 0) *issued_tiles = j;
     } else if (warp == PF_MMA_WARP) {
         // ---------------------------------------------------------------- MMA issue
         const uint32_t idesc_s = umma_idesc<T>(PF_BM, PF_BN, false);
         const uint32_t idesc_o = umma_idesc<T>(PF_BM, PF_D, true);
-        auto issue_pv = [&](int t, int j) {                   // O_t += P_t V(j)
-            const uint32_t vst = base + LY::OFF_STAGE + (j % STAGES) * PF_STAGE_BYTES + PF_KV_BYTES;
+        // Shared-memory descriptors are built once; per MMA only a constant (address >> 4) is added
+        // (every operand lies below 256 KB, so the 14-bit address field never carries).
+        const uint64_t dq0 = umma_desc_sw128(base, 16, 1024);
+        const uint64_t dk0 = umma_desc_sw128(base + LY::OFF_STAGE, 16, 1024);
+        const uint64_t dv0 = umma_desc_sw128(base + LY::OFF_STAGE + PF_KV_BYTES, PF_BN * 128, 1024);
+        auto issue_pv = [&](int t, int j) {                   // O_t += P_t(j) V(j), P in TMEM buffer j & 1
+            const uint64_t dv = dv0 + (uint64_t)((j % STAGES) * (PF_STAGE_BYTES >> 4));
+            const uint32_t pt = tmem + t * 256 + (j & 1) * PF_BN, ot = tmem + t * 256 + 128;
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int part = 0; part < (SPLIT_P ? 2 : 1); ++part) {
 #pragma unroll
-                for (int ks = 0; ks < PF_BN / 16; ++ks) {
-                    const uint32_t pa = base + LY::OFF_P + t * LY::P_TILE + part * PF_P_BYTES + ks * 32;
-                    const uint32_t va = vst + ks * 16 * 128;
-                    umma_f16(tmem + 128 + t * 128, umma_desc_sw128(pa, 16, 1024),
-                             umma_desc_sw128(va, PF_BN * 128, 1024), idesc_o, (j > 0 || ks > 0 || part > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < PF_BN / 16; ++ks)
+                    umma_f16_tmem_a(ot, pt + part * 32 + ks * 8, dv + (uint64_t)((ks * 16 * 128) >> 4), idesc_o,
+                                    (ks > 0 || part > 0) ? 1u : acc0);
             }
+            umma_commit(bar_o_bar + (t * 2 + (j & 1)) * 8);
         };
         auto wait_p = [&](int t, int j) -> bool {            // softmax of row tile t wrote P(j)
-            const bool got = mbar_wait_bounded(bar_p_full + t * 8, (uint32_t)j & 1u, p.wait_ns);
+            const bool got =
+                mbar_wait_bounded(bar_p_full + (t * 2 + (j & 1)) * 8, (uint32_t)(j >> 1) & 1u, p.wait_ns);
             return __all_sync(0xffffffffu, got);
         };
         bool ok = true;
@@ -227,30 +235,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            const uint32_t kst = base + LY::OFF_STAGE + st * PF_STAGE_BYTES;
+            // S(t, j) into buffer j & 1 (its last reader, P(j-2).V, was issued one tile earlier)
+            if (lane == 0) {
+                const uint64_t dk = dk0 + (uint64_t)(st * (PF_STAGE_BYTES >> 4));
+                tc_fence_after();
 #pragma unroll
-            for (int t = 0; t < PF_QT; ++t) {
-                if (j > 0 && j - 1 < nt_of[t]) {
-                    if (!(ok = wait_p(t, j - 1))) break;
-                    if (lane == 0) {
-                        tc_fence_after();
-                        issue_pv(t, j - 1);
-                    }
-                }
-                if (j < nt_of[t] && lane == 0) {
-                    tc_fence_after();
+                for (int t = 0; t < PF_QT; ++t) {
+                    if (j < nt_of[t]) {
+                        const uint64_t dq = dq0 + (uint64_t)(t * (PF_Q_BYTES >> 4));
+                        const uint32_t sd = tmem + t * 256 + (j & 1) * PF_BN;
 #pragma unroll
-                    for (int ks = 0; ks < PF_D / 16; ++ks) {
-                        const uint32_t qa = base + t * PF_Q_BYTES + (ks >> 2) * (PF_BM * 128) + (ks & 3) * 32;
-                        const uint32_t ka = kst + (ks >> 2) * (PF_BN * 128) + (ks & 3) * 32;
-                        umma_f16(tmem + t * PF_BN, umma_desc_sw128(qa, 16, 1024), umma_desc_sw128(ka, 16, 1024),
-                                 idesc_s, ks > 0);
+                        for (int ks = 0; ks < PF_D / 16; ++ks)
+                            umma_f16(sd, dq + (uint64_t)(((ks >> 2) * (PF_BM * 128) + (ks & 3) * 32) >> 4),
+                                     dk + (uint64_t)(((ks >> 2) * (PF_BN * 128) + (ks & 3) * 32) >> 4), idesc_s,
+                                     ks > 0 ? 1u : 0u);
+                        umma_commit(bar_s_full + (t * 2 + (j & 1)) * 8);
                     }
-                    umma_commit(bar_s_full + t * 8);
                 }
             }
-            if (!ok) break;
-            if (j > 0 && lane == 0) umma_commit(bar_kv_empty + ((j - 1) % STAGES) * 8);
+            // P(t, j-1) V(j-1) once the softmax of row tile t has written P(j-1)
+            if (j > 0) {
+#pragma unroll
+                for (int t = 0; t < PF_QT; ++t) {
+                    if (j - 1 < nt_of[t]) {
+                        if (!(ok = wait_p(t, j - 1))) break;
+                        if (lane == 0) {
+                            tc_fence_after();
+                            issue_pv(t, j - 1);
+                        }
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) umma_commit(bar_kv_empty + ((j - 1) % STAGES) * 8);
+            }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) ok = false;
         }
         if (ok && ntiles > 0) {
@@ -273,32 +290,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int t = t_of;
         const int nt = t ? nt_of[1] : nt_of[0];
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tmem_s = tmem + t * PF_BN + lane_base, tmem_o = tmem + 128 + t * 128 + lane_base;
+        const uint32_t tmem_t = tmem + t * 256 + lane_base, tmem_o = tmem_t + 128;
         const int lim = L - p.q_len + qi;                      // last key this row may see
-        uint8_t *ph = smem + LY::OFF_P + t * LY::P_TILE + rt * 128;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_s_full + t * 8, (uint32_t)j & 1u, p.wait_ns));
+            const int buf = j & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_s_full + (t * 2 + buf) * 8, (uint32_t)(j >> 1) & 1u,
+                                                           p.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float sv[PF_BN];
-            tmem_ld64(tmem_s, sv);
+            tmem_ld64(tmem_t + buf * PF_BN, sv);
+            // raw-score max (the scale is positive, so it commutes with the max); eight independent
+            // partial maxima and sums keep the dependent chains short
             const int t0 = j * PF_BN;
-            float mx = -INFINITY;
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
             if (t0 + PF_BN - 1 <= lim) {
 #pragma unroll
-                for (int c = 0; c < PF_BN; ++c) {
-                    sv[c] *= p.scale_log2;
-                    mx = fmaxf(mx, sv[c]);
-                }
+                for (int c = 0; c < PF_BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
             } else {
 #pragma unroll
                 for (int c = 0; c < PF_BN; ++c) {
-                    sv[c] = t0 + c <= lim ? sv[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
+                    sv[c] = t0 + c <= lim ? sv[c] : -INFINITY;
+                    m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * p.scale_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_ref + PF_RESCALE_LOG2 || (m_ref == -INFINITY && mx > -INFINITY)) {
@@ -306,16 +327,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 m_ref = mx;
                 rescale = true;
             }
-            const float muse = m_ref == -INFINITY ? 0.f : m_ref;
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < PF_BN; ++c) {
-                sv[c] = ex2_approx(sv[c] - muse);
-                rs += sv[c];
-            }
-            l = l * alpha + rs;
-            // P.V of the previous key tile completed before S of this one (same commit)
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // O holds the sums through key tile j-1: wait for P(j-1).V, then scale this warp's rows
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_o_bar + (t * 2 + (buf ^ 1)) * 8,
+                                                               (uint32_t)((j - 1) >> 1) & 1u, p.wait_ns));
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < PF_D; c0 += 32) {
                     float a[32];
@@ -325,28 +342,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     tmem_st32(tmem_o + c0, a);
                 }
             }
-            // P -> shared memory, K-major operand layout: this row's 64 keys are one 128-byte row
+            const float nmuse = m_ref == -INFINITY ? 0.f : -m_ref;
+            float r8[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4], wl[4];
+            for (int i = 0; i < 8; ++i) r8[i] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = sv[c * 8 + 2 * e], x1 = sv[c * 8 + 2 * e + 1];
-                    w[e] = pack2<T>(x0, x1);
-                    if constexpr (SPLIT_P) {
-                        // bf16 hi parts back to fp32 (a bf16 is the top half of an fp32), then lo = x - hi
-                        const float h0 = __uint_as_float(w[e] << 16), h1 = __uint_as_float(w[e] & 0xFFFF0000u);
-                        wl[e] = pack2<T>(x0 - h0, x1 - h1);
-                    }
-                }
-                const int pos = (c ^ (rt & 7)) << 4;
-                *reinterpret_cast<uint4 *>(ph + pos) = make_uint4(w[0], w[1], w[2], w[3]);
-                if constexpr (SPLIT_P)
-                    *reinterpret_cast<uint4 *>(ph + PF_P_BYTES + pos) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            for (int c = 0; c < PF_BN; ++c) {
+                sv[c] = ex2_approx(fmaf(sv[c], p.scale_log2, nmuse));
+                r8[c & 7] += sv[c];
             }
-            fence_proxy_async_smem();
+            l = l * alpha + ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+            // P over this buffer's S: 64 keys as 32 packed columns (bf16: hi, then lo = x - hi)
+            {
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) w[c] = pack2<T>(sv[2 * c], sv[2 * c + 1]);
+                tmem_st32_raw(tmem_t + buf * PF_BN, w);
+                if constexpr (SPLIT_P) {
+                    uint32_t wl[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        // a bf16 is the top half of an fp32
+                        const float h0 = __uint_as_float(w[c] << 16), h1 = __uint_as_float(w[c] & 0xFFFF0000u);
+                        wl[c] = pack2<T>(sv[2 * c] - h0, sv[2 * c + 1] - h1);
+                    }
+                    tmem_st32_raw(tmem_t + buf * PF_BN + 32, wl);
+                }
+                tmem_wait_st();
+            }
             tc_fence_before();
-            mbar_arrive(bar_p_full + t * 8);
+            mbar_arrive(bar_p_full + (t * 2 + buf) * 8);
             if (__any_sync(0xffffffffu, *abort_flag != 0)) {
                 ok = false;
                 break;

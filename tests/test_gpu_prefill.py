@@ -81,6 +81,9 @@ def test_prefill_deterministic_and_rejects():
     bad[0] = 100
     pool.prefill(q, tables, bad, wl.scale, k_cache=kc, v_cache=vc)
     assert pool.check() == pa.PA_ERR_DEVICE_BOUNDS
+    # the softmax scale must be positive
+    with pytest.raises(RuntimeError):
+        pool.prefill(q, tables, lens, -wl.scale, k_cache=kc, v_cache=vc)
     # head_dim 64 pools are not supported by the prefill path
     small = pa.Pool(16, 16, 2, 64, torch.float16, 0, max_seqs=1, max_q_heads=4, max_q_len=1, max_context_len=256)
     q64 = torch.zeros((1, 4, 4, 64), dtype=torch.float16, device=H.DEV)
