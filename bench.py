@@ -9,6 +9,7 @@ KV, far larger than L2, so no flush is needed between steps).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3|cfg5|cfg2|cfg4|cfg1]
     python bench.py --impl reference      # the fp64 CPU oracle as the reference arm
+    python bench.py --workload prefill    # chunked prefill (pa_prefill), tensor-core bound: TFLOP/s
 
 Under torchrun each rank runs the same workload on its own GPU (weak scaling, no collective
 on the data path); the time is the maximum over ranks.
@@ -32,14 +33,17 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 import synth  # noqa: E402
 
-WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5}
+WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "prefill": 0}
 DESCR = {
     1: "tiny paged decode (B4, lens 17/64/100/200, Hq8 Hkv2 d64 bs16, fp16)",
     2: "Llama-3-8B-shaped decode layer (B64, lens U[512,4096], Hq32 Hkv8 d128 bs16, bf16)",
     3: "Llama-3-70B-shaped decode, 80 layer pools (B64, ctx 8192, Hq64 Hkv8 d128 bs16, fp16)",
     4: "shared 1024-token prefix + 5-token causal verify (B128, suffix U[64,512], Hq32 Hkv8 d128 bs16, bf16)",
     5: "long-context split decode (B4, ctx 131072, Hq32 Hkv8 d128 bs32, fp16, 512-token partitions)",
+    0: "chunked prefill, Llama-3-70B-shaped: 8 sequences each attending with a 512-token chunk that ends at "
+       "context 4608 (the 9th chunk of the prompt), Hq64 Hkv8 d128 bs16, 8 layer pools",
 }
+PREFILL = dict(batch=8, chunk=512, context=4608, layers=8)
 
 
 def dist_env():
@@ -318,6 +322,186 @@ def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier, kv_for
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3), "steps": steps}
 
 
+# ------------------------------------------------------------------------------------- chunked prefill
+
+def prefill_workload(layer: int, dtype: int, batch: int = PREFILL["batch"]) -> synth.Workload:
+    """One layer pool of the prefill workload: every sequence's chunk ends at the same context length; each layer
+    has its own seed and block placement."""
+    return synth.custom_workload([PREFILL["context"]] * batch, 64, 8, 128, 16, PREFILL["chunk"], dtype,
+                                 tag=500 + layer)
+
+
+def prefill_flops(wl: synth.Workload) -> int:
+    """Algorithmic FLOPs of one pa_prefill call: QK^T and PV (2 FLOPs per multiply-add each) over the causal
+    (row, key) pairs: chunk row qi of sequence b sees L_b - C + qi + 1 keys."""
+    C = wl.q_len
+    pairs = sum(C * (int(L) - C) + C * (C + 1) // 2 for L in wl.context_lens)
+    return 4 * wl.d * wl.Hq * pairs
+
+
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (bf16 dense burst; fp16 runs at the same nominal rate)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+class PrefillLayers:
+    """Per-layer pools with every token but the chunk written; the step writes the chunk and runs pa_prefill."""
+
+    def __init__(self, layers: int, dtype: int, dev, batch: int):
+        import torch
+        import gpu_harness as H
+        import synth.device as sdev
+        self.layers = []
+        self.pool = None
+        for layer in range(layers):
+            wl = prefill_workload(layer, dtype, batch)
+            kc, vc = H.alloc_caches(wl)
+            if self.pool is None:
+                self.pool = H.make_pool(wl, 0, kc, vc)
+            H.fill(self.pool, wl, 0, kc, vc, new_only=False)
+            (kind, rows, slots), = wl.write_plan(new_only=True)
+            kn, vn = sdev.kv_rows(wl, 0, kind, torch.from_numpy(rows).to(dev), dev)
+            q, tables, lens = H.device_inputs(wl, 0)
+            self.layers.append(dict(wl=wl, kc=kc, vc=vc, kn=kn, vn=vn, slots=torch.from_numpy(slots).to(dev), q=q,
+                                    tables=tables, lens=lens, out=torch.empty_like(q)))
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        for i, L in enumerate(self.layers):
+            self.pool.cache_write(L["kn"], L["vn"], L["slots"], L["kc"], L["vc"])
+            if events is not None:
+                events[i][0].record()
+            self.pool.prefill(L["q"], L["tables"], L["lens"], L["wl"].scale, out=L["out"], k_cache=L["kc"],
+                              v_cache=L["vc"])
+            if events is not None:
+                events[i][1].record()
+
+
+def prefill_cpu_baseline(wl: synth.Workload, seconds: float):
+    """The oracle on sequence prefixes of layer 0: cache write of the chunk + fp64 paged attention with
+    q_len = chunk, as many sequences as fit in about `seconds` (at least one)."""
+    import oracle
+    done, flops, threads, t_total = 0, 0, 0, 0.0
+    while done < wl.B and (done == 0 or t_total < seconds):
+        hk, hv, news, q = oracle_sample(wl, done + 1)
+        t0 = time.perf_counter()
+        kn, vn, sl = news[done]
+        oracle.cache_write(hk, hv, kn, vn, sl)
+        _, threads = oracle.paged_attention(q[done:done + 1], hk, hv, wl.block_tables[done:done + 1],
+                                            wl.context_lens[done:done + 1], wl.dtype, wl.scale)
+        t_total += time.perf_counter() - t0
+        sub = synth.Workload(**{**wl.__dict__, "B": 1, "context_lens": wl.context_lens[done:done + 1]})
+        flops += prefill_flops(sub)
+        done += 1
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"layer 0, sequences 0..{done - 1} of the prefill workload: chunk cache write + fp64 paged "
+                      f"attention with q_len {wl.q_len} ({flops} algorithmic FLOPs) in {t_total:.2f} s"}
+
+
+def run_prefill(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dtype = synth.DTYPES[args.dtype]
+    batch = args.batch or PREFILL["batch"]
+    layers = args.layers or PREFILL["layers"]
+    P = PrefillLayers(layers, dtype, dev, batch)
+    flops_call = prefill_flops(P.layers[0]["wl"])
+    flops_step = flops_call * layers
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        P.step()
+    barrier()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.3)
+        barrier()
+        start.record()
+        for s in range(args.steps):
+            P.step(evs[s])
+        stop.record()
+        barrier()
+    elapsed_ms = reduce_max(start.elapsed_time(stop), dev)
+    call_ms = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps) for i in range(layers)]
+    assert P.pool.check() == 0, "device status flagged during the prefill benchmark"
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for L in P.layers:
+            host.append({k: L[k].cpu().pin_memory() for k in ("kn", "vn", "slots", "q", "tables", "lens")})
+            host[-1]["out"] = torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for hl in host for k, t in hl.items() if k != "out")
+        d2h = sum(hl["out"].numel() * hl["out"].element_size() for hl in host)
+
+        def one():
+            for L, hl in zip(P.layers, host):
+                for k in ("kn", "vn", "slots", "q", "tables", "lens"):
+                    L[k].copy_(hl[k], non_blocking=True)
+                P.pool.cache_write(L["kn"], L["vn"], L["slots"], L["kc"], L["vc"])
+                P.pool.prefill(L["q"], L["tables"], L["lens"], L["wl"].scale, out=L["out"], k_cache=L["kc"],
+                               v_cache=L["vc"])
+                hl["out"].copy_(L["out"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        one()
+        barrier()
+        n = max(3, args.steps // 5)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            one()
+        barrier()
+        dt = (time.perf_counter() - t0) / n
+        e2e = {"value": round(ws * flops_step / dt / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3), "steps": n}
+    if rank == 0:
+        peak, peak_kind = tensor_peak()
+        call_avg = float(np.mean(call_ms))
+        achieved = flops_call / (call_avg * 1e-3) / 1e12
+        wl0 = P.layers[0]["wl"]
+        line = {
+            "metric": "chunked-prefill attention TFLOP/s on 1 GB300 (fraction of dense tensor peak)",
+            "value": round(ws * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": args.dtype, "data": "synthetic (seeded, N(0,1)-shaped)",
+            "config": {**synth.describe(wl0), "workload": f"prefill: {DESCR[0]}", "layers": layers,
+                       "l2": "8 layer pools (1.2 GB of K/V) cycle through L2 (no flush)",
+                       "parallelism": f"replicas{ws}"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "pa_prefill call (prefill kernel)", "algorithmic_flops_per_launch": flops_call,
+                         "avg_launch_ms": round(call_avg, 5), "peak_kind": peak_kind},
+            "e2e": e2e,
+            "gpu_launches": 2 * layers * args.steps,
+            "clocks": clk.summary(),
+        }
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = prefill_cpu_baseline(prefill_workload(0, dtype, batch), args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------------------------- CPU oracle arm
 
 def oracle_sample(wl: synth.Workload, nseq: int):
@@ -388,6 +572,9 @@ def run_reference(args):
         return
     import oracle
     k = WORKLOADS[args.workload]
+    if k == 0:
+        run_prefill_reference(args)
+        return
     wl = synth.workload(k, layers=1)
     nseq = pick_nseq(wl, args.ref_step_seconds)
     hk, hv, news, q = oracle_sample(wl, nseq)
@@ -415,6 +602,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_reference(args):
+    """The oracle as the prefill reference arm: each step is one bounded sample of the workload."""
+    ws = dist_env()[0]
+    wl = prefill_workload(0, synth.DTYPES[args.dtype], args.batch or PREFILL["batch"])
+    for _ in range(args.warmup):
+        prefill_cpu_baseline(wl, 0.0)
+    vals = [prefill_cpu_baseline(wl, args.ref_step_seconds) for _ in range(args.steps)]
+    value = round(float(np.mean([v["value"] for v in vals])), 6)
+    line = {"impl": "reference",
+            "metric": "chunked-prefill attention TFLOP/s on 1 GB300 (fraction of dense tensor peak)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, N(0,1)-shaped)",
+            "config": {**synth.describe(wl), "workload": f"prefill: {DESCR[0]}"},
+            "cpu_baseline": {**vals[-1], "value": value},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -427,13 +633,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"], help="KV cache storage")
-    ap.add_argument("--layers", type=int, default=None, help="layer pools (workload 3 only; default 80)")
+    ap.add_argument("--layers", type=int, default=None, help="layer pools (cfg3: default 80; prefill: default 8)")
     ap.add_argument("--batch", type=int, default=None, help="sequences (default: the workload's)")
+    ap.add_argument("--dtype", default="fp16", choices=sorted(synth.DTYPES), help="prefill workload dtype")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_gpu(args)
 
