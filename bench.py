@@ -145,7 +145,7 @@ class ClockSampler:
 class GpuWorkload:
     """Every layer's pool filled through pa_cache_write; per-layer inputs resident on the device."""
 
-    def __init__(self, wl: synth.Workload, dev, kv_format: int = 0):
+    def __init__(self, wl: synth.Workload, dev, kv_format: int = 0, shared_prefix: bool = False):
         import torch
         import gpu_harness as H
         import synth.device as sdev
@@ -164,7 +164,17 @@ class GpuWorkload:
             self.layers.append(dict(kc=kc, vc=vc, kn=kn, vn=vn, slots=torch.from_numpy(slots).to(dev), q=q,
                                     tables=tables, lens=lens, out=torch.empty_like(q)))
         torch.cuda.synchronize()
-        self.decode_launches = self.pool.launches(wl.stride, wl.B, wl.Hq, wl.q_len)
+        self.shared_prefix = shared_prefix and wl.prefix_tokens > 0
+        # pa_decode_shared_prefix: prefix kernel + suffix decode + merge
+        self.decode_launches = 3 if self.shared_prefix else self.pool.launches(wl.stride, wl.B, wl.Hq, wl.q_len)
+
+    def decode(self, L):
+        wl = self.wl
+        if self.shared_prefix:
+            self.pool.decode_shared_prefix(L["q"], L["tables"], L["lens"], wl.scale, wl.prefix_tokens, out=L["out"],
+                                           k_cache=L["kc"], v_cache=L["vc"])
+        else:
+            self.pool.decode(L["q"], L["tables"], L["lens"], wl.scale, out=L["out"], k_cache=L["kc"], v_cache=L["vc"])
 
     def step(self, events=None):
         wl = self.wl
@@ -172,7 +182,7 @@ class GpuWorkload:
             self.pool.cache_write(L["kn"], L["vn"], L["slots"], L["kc"], L["vc"])
             if events is not None:
                 events[i][0].record()
-            self.pool.decode(L["q"], L["tables"], L["lens"], wl.scale, out=L["out"], k_cache=L["kc"], v_cache=L["vc"])
+            self.decode(L)
             if events is not None:
                 events[i][1].record()
 
@@ -219,7 +229,7 @@ def run_gpu(args):
     k = WORKLOADS[args.workload]
     wl = synth.workload(k, layers=args.layers, batch=args.batch)
     kv_format = 1 if args.kv == "fp8" else 0
-    G = GpuWorkload(wl, dev, kv_format)
+    G = GpuWorkload(wl, dev, kv_format, args.shared_prefix)
     total_bytes, decode_bytes = step_bytes(wl, kv_format)
     kv_tokens = int(wl.context_lens.sum()) * wl.layers
 
@@ -268,6 +278,7 @@ def run_gpu(args):
             "dtype": ("fp16" if wl.dtype == synth.FP16 else "bf16") + ("+fp8-kv" if kv_format else ""),
             "data": "synthetic (seeded, N(0,1)-shaped)",
             "config": {**synth.describe(wl), "workload": f"{args.workload}: {DESCR[k]}",
+                       "decode_call": "pa_decode_shared_prefix" if G.shared_prefix else "pa_decode",
                        "kv_cache": "fp8 e4m3 + fp32 scale per (slot, head)" if kv_format else "16-bit",
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{ws}"},
             "kv_tokens_per_s": round(ws * kv_tokens * args.steps / (elapsed_ms * 1e-3), 1),
@@ -275,7 +286,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": None if kv_format else measured_traffic(args.workload),
-                         "kernel": "pa_decode call (decode kernel + partition merge)",
+                         "kernel": ("pa_decode_shared_prefix call (prefix kernel + suffix decode + merge)"
+                                    if G.shared_prefix else "pa_decode call (decode kernel + partition merge)"),
                          "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                          "peak_kind": peak_kind},
             "e2e": e2e,
@@ -305,7 +317,7 @@ def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier, kv_for
             for k in ("kn", "vn", "slots", "q", "tables", "lens"):
                 L[k].copy_(hl[k], non_blocking=True)
             G.pool.cache_write(L["kn"], L["vn"], L["slots"], L["kc"], L["vc"])
-            G.pool.decode(L["q"], L["tables"], L["lens"], wl.scale, out=L["out"], k_cache=L["kc"], v_cache=L["vc"])
+            G.decode(L)
             hl["out"].copy_(L["out"], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -636,6 +648,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="layer pools (cfg3: default 80; prefill: default 8)")
     ap.add_argument("--batch", type=int, default=None, help="sequences (default: the workload's)")
     ap.add_argument("--dtype", default="fp16", choices=sorted(synth.DTYPES), help="prefill workload dtype")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="decode workloads with a shared prefix (cfg4) through pa_decode_shared_prefix")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3

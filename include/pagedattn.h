@@ -154,6 +154,30 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
                     void *stream);
 
 /*
+ * Paged decode for a batch whose sequences share a prefix (copy-on-write
+ * blocks named by every table: yangyu.win blog #54, section 5 question 2;
+ * itimpress.au section 1). Computes exactly pa_decode's result; the shared
+ * part is evaluated once for the whole batch: every query row of every
+ * sequence attends to each prefix partition on the 5th-generation tensor
+ * cores (one pass over the prefix's K/V instead of one per sequence), the
+ * decode kernel covers each sequence's own tokens, and the log-sum-exp merge
+ * combines the partitions (maths.nthquan ch. 17 "Sequence parallelism").
+ * Preconditions, checked on the device (violations are flagged,
+ * PA_ERR_DEVICE_BOUNDS at pa_pool_check, outputs then unspecified):
+ *   block_tables[b][i] == block_tables[0][i] for i < prefix_tokens / block_size;
+ *   context_lens[b] - q_len >= prefix_tokens (every query row follows the prefix).
+ * Host-checked: 16-bit pool, head_dim 128, the pool's partition_tokens a
+ * multiple of 128, prefix_tokens a positive multiple of partition_tokens and
+ * below the launch's longest context, scale > 0; all other arguments as
+ * pa_decode (which this call replaces; it uses the pool's workspace).
+ */
+pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, int32_t block_table_stride,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t q_len, float scale, int32_t prefix_tokens, void *out,
+                                  void *stream);
+
+/*
  * Chunked prefill: attention for a chunk of q_len new tokens per sequence, the
  * chunk's K and V already written to the pool (pa_cache_write). A long prompt
  * is processed in chunks (yangyu.win blog #54, section 4 "Chunked Prefill":

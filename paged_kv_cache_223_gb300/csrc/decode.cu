@@ -116,8 +116,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int part = blockIdx.x % p.max_parts;
-    const int bg = blockIdx.x / p.max_parts;
+    const int nlaunch = p.max_parts - p.part0;         // partitions launched per (sequence, KV head)
+    const int part = p.part0 + (int)(blockIdx.x % nlaunch);
+    const int bg = blockIdx.x / nlaunch;
     const int g = bg % p.Hkv;
     const int b = bg / p.Hkv;
 
@@ -126,6 +127,17 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     if (L < p.q_len || L > p.max_ctx) {
         if (threadIdx.x == 0 && part == 0) set_status(p.status, STATUS_BOUNDS);
         L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+    }
+    if (p.part0 > 0 && part == p.part0 && g == 0) {
+        // shared-prefix decode: the prefix kernel read sequence 0's blocks for every sequence and
+        // assumed that every query row follows the whole prefix; check both for this sequence
+        const int pre_blocks = p.part0 * p.part_tokens / p.bs;
+        if (L - p.q_len < p.part0 * p.part_tokens) {
+            if (threadIdx.x == 0) set_status(p.status, STATUS_BOUNDS);
+        }
+        for (int i = threadIdx.x; i < pre_blocks; i += blockDim.x)
+            if (__ldg(p.block_tables + (int64_t)b * p.stride + i) != __ldg(p.block_tables + i))
+                set_status(p.status, STATUS_BOUNDS);
     }
     const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
     if (part >= nparts) return;
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     }
     __syncthreads();
 
-    const bool direct = nparts == 1;
+    const bool direct = nparts == 1 && p.part0 == 0;
     for (int idx = threadIdx.x; idx < p.rows * (D / 2); idx += blockDim.x) {
         const int r = idx / (D / 2);
         const int dp = (idx - r * (D / 2)) * 2;
@@ -603,7 +615,7 @@ static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tmk
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)p.num_seqs * p.Hkv * p.max_parts;
+    const int64_t grid = (int64_t)p.num_seqs * p.Hkv * (p.max_parts - p.part0);
     decode_kernel<T, D, NT, KV8><<<(unsigned)grid, DECODE_WARPS * 32, smem, stream>>>(tmk, tmv, p);
     return cudaGetLastError();
 }

@@ -24,6 +24,9 @@ struct pa_pool {
     int sm_count = 0;
     int part_tokens = 512;
     uint64_t wait_ns = 2000000000ull;
+    // shared-prefix decode: the prefix kernel runs on this stream beside the caller's decode
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     std::mutex mu;
     std::unordered_map<const void *, CUtensorMap> maps;
 };
@@ -99,6 +102,9 @@ void free_pool(pa_pool *p) {
     cudaFree(p->part_o);
     cudaFree(p->part_ml);
     cudaFree(p->status);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->side) cudaStreamDestroy(p->side);
     delete p;
 }
 
@@ -175,6 +181,13 @@ pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out) {
         cudaGetLastError();
         free_pool(p);
         return PA_ERR_OOM;
+    }
+    if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        free_pool(p);
+        return PA_ERR_CUDA;
     }
     *out = p;
     return PA_OK;
@@ -302,6 +315,68 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s, kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t q_len, float scale,
+                                  int32_t prefix_tokens, void *out, void *stream) {
+    if (!pool || !q || !out || !block_tables || !context_lens || !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return PA_ERR_INVALID_ARG;
+    const pa_pool_config &c = pool->cfg;
+    if (c.kv_format != PA_KV_16BIT || c.head_dim != 128 || pool->part_tokens % 128 != 0) return PA_ERR_UNSUPPORTED;
+    if (!k_cache) {
+        k_cache = pool->k_cache;
+        v_cache = pool->v_cache;
+    }
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams p;
+    pa_status st = decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p);
+    if (st != PA_OK) return st;
+    if (prefix_tokens <= 0 || prefix_tokens % pool->part_tokens != 0 || prefix_tokens / pool->part_tokens >= p.max_parts)
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * p.rows > ((int64_t)1 << 24)) return PA_ERR_UNSUPPORTED;
+    p.part0 = prefix_tokens / pool->part_tokens;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_scales = p.v_scales = nullptr;
+    DeviceGuard g(c.device);
+    if (!g.ok) return PA_ERR_CUDA;
+    CUtensorMap tmk, tmv;
+    if ((st = tensor_map(pool, k_cache, &tmk)) != PA_OK) return st;
+    if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
+    // prefix partitions per prefix CTA: the fewest waves of (partitions per CTA + 2 tiles of start-up)
+    {
+        const int64_t ctiles = (((int64_t)num_seqs * p.rows + 127) / 128 + 1) / 2;
+        const int tiles_per_part = pool->part_tokens / 128;
+        int64_t best = -1;
+        for (int k = 1; k <= p.part0; ++k) {
+            const int64_t ctas = ctiles * p.Hkv * ((p.part0 + k - 1) / k);
+            const int64_t cost = ((ctas + pool->sm_count - 1) / pool->sm_count) * (k * tiles_per_part + 2);
+            if (best < 0 || cost < best) {
+                best = cost;
+                p.pchunk = k;
+            }
+        }
+    }
+    // the prefix kernel (tensor cores, one CTA per SM) runs on the pool's side stream beside the suffix
+    // decode (bandwidth, many small CTAs) on the caller's stream; the merge waits for both
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lk(pool->mu);
+    if (cudaEventRecord(pool->ev_fork, s) != cudaSuccess || cudaStreamWaitEvent(pool->side, pool->ev_fork, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (launch_prefix(p, c.dtype, tmk, tmv, pool->side) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_decode(p, c.dtype, c.head_dim, tmk, tmv, s, false) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaEventRecord(pool->ev_join, pool->side) != cudaSuccess || cudaStreamWaitEvent(s, pool->ev_join, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (launch_merge(p, c.dtype, c.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
 

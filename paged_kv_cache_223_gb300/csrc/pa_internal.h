@@ -41,6 +41,9 @@ struct DecodeParams {
     int max_ctx;         // longest context the launch covers (max_parts * part_tokens, <= stride * bs)
     float scale_log2;    // scale * log2(e)
     uint64_t wait_ns;    // bounded-wait limit
+    int part0 = 0;       // shared-prefix decode: partitions below part0 (the prefix) come from the prefix
+                         // kernel; the decode covers [part0, max_parts)
+    int pchunk = 1;      // prefix partitions per prefix-kernel CTA (their combined state goes to the first)
 };
 
 struct CacheWriteParams {
@@ -74,6 +77,10 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n, void *k_cache, v
                                int32_t num_blocks, int *status, int sm_count, cudaStream_t stream);
 cudaError_t launch_prefill(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            cudaStream_t stream);
+// Shared-prefix attention: every query row of every sequence against prefix partitions [0, part0)
+// (blocks from sequence 0's table), written as partition partials for the merge.
+cudaError_t launch_prefix(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                          cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int nt);
 size_t prefill_smem_bytes();
 size_t merge_smem_bytes(int G, int max_parts, int head_dim);

@@ -21,6 +21,12 @@
 //                      S from TMEM, causal mask, running max (the O rescale is skipped while the
 //                      max grows by less than 2^8), row sum, P (bf16: hi + lo parts) written back to
 //                      TMEM over the S it came from
+// The same kernel (CASCADE) computes a shared prefix once for a whole batch: its rows are every
+// sequence's query rows, its keys one partition of the prefix (blocks from sequence 0's table, no
+// mask: every query row follows the prefix), and it writes the unnormalised partition state
+// (O, running max, sum) that the log-sum-exp merge combines with the decode of each suffix
+// (a cascade over the pages' copy-on-write prefix blocks: yangyu.win blog #54 section 5
+// question 2, itimpress.au section 1).
 // Tensor memory per row tile: S/P (128 columns) and O (128 columns). MMAs of one thread execute in
 // issue order, so S(j) overwrites P(j-1) only after P(j-1).V has read it, and the commit of S(j)
 // also covers P(j-1).V: the softmax of tile j may rescale O without another wait.
@@ -59,7 +65,7 @@ static_assert(PF_SMEM <= 227 * 1024, "prefill shared memory");
 
 size_t prefill_smem_bytes() { return PF_SMEM; }
 
-template <typename T>
+template <typename T, bool CASCADE>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const DecodeParams p) {
@@ -81,16 +87,28 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     volatile int *issued_tiles = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [K, V]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mtiles = (p.rows + PF_BM - 1) / PF_BM;
+    const int total_rows = CASCADE ? p.num_seqs * p.rows : p.rows;   // query rows of one CTA's unit
+    const int mtiles = (total_rows + PF_BM - 1) / PF_BM;
     const int ctiles = (mtiles + PF_QT - 1) / PF_QT;
     const int ct = ctiles - 1 - (int)(blockIdx.x % ctiles);  // the unit's longest row tiles start first
-    const int bg = blockIdx.x / ctiles;
-    const int g = bg % p.Hkv, b = bg / p.Hkv;
-
-    int L = __ldg(p.context_lens + b);
-    if (L < p.q_len || L > p.max_ctx) {
-        if (tid == 0 && ct == 0) set_status(p.status, STATUS_BOUNDS);
-        L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+    const int unit = blockIdx.x / ctiles;
+    const int g = unit % p.Hkv;
+    // b: the sequence whose table names the keys; the keys are tokens [key0, L)
+    int b, key0, L;
+    if constexpr (CASCADE) {
+        // prefix partitions [c * pchunk, min((c + 1) * pchunk, part0)) of chunk c
+        b = 0;
+        const int c = unit / p.Hkv;
+        key0 = c * p.pchunk * p.part_tokens;
+        L = min((c + 1) * p.pchunk, p.part0) * p.part_tokens;
+    } else {
+        b = unit / p.Hkv;
+        key0 = 0;
+        L = __ldg(p.context_lens + b);
+        if (L < p.q_len || L > p.max_ctx) {
+            if (tid == 0 && ct == 0) set_status(p.status, STATUS_BOUNDS);
+            L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+        }
     }
     // key tiles each row tile needs: up to the last key its last row sees
     int nt0, nt1;
@@ -99,10 +117,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
         for (int t = 0; t < PF_QT; ++t) {
             const int mt = ct * PF_QT + t;
-            int last_q = (mt * PF_BM + PF_BM - 1) / p.G;
-            if (last_q > p.q_len - 1) last_q = p.q_len - 1;
-            const int kv_end = L - p.q_len + last_q + 1;
-            nt[t] = (mt < mtiles && kv_end > 0) ? (kv_end + PF_BN - 1) / PF_BN : 0;
+            if constexpr (CASCADE) {
+                nt[t] = mt < mtiles ? (L - key0) / PF_BN : 0;
+            } else {
+                int last_q = (mt * PF_BM + PF_BM - 1) / p.G;
+                if (last_q > p.q_len - 1) last_q = p.q_len - 1;
+                const int kv_end = L - p.q_len + last_q + 1;
+                nt[t] = (mt < mtiles && kv_end > 0) ? (kv_end + PF_BN - 1) / PF_BN : 0;
+            }
         }
         nt0 = nt[0];
         nt1 = nt[1];
@@ -134,12 +156,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // softmax threads: row tile t = tid / 128, row rt = tid % 128
     const int t_of = tid >> 7, rt = tid & (PF_BM - 1);
     const int r = (ct * PF_QT + t_of) * PF_BM + rt;
-    const bool row_ok = tid < PF_SM_THREADS && r < p.rows;
-    const int qi = row_ok ? r / p.G : p.q_len - 1;
-    const int hh = row_ok ? r - (r / p.G) * p.G : 0;
+    const bool row_ok = tid < PF_SM_THREADS && r < total_rows;
+    const int rb = CASCADE ? (row_ok ? r / p.rows : 0) : b;   // this row's sequence
+    const int rr = row_ok ? r - (CASCADE ? rb * p.rows : 0) : p.rows - 1;
+    const int qi = rr / p.G;
+    const int hh = rr - qi * p.G;
+    const int64_t orow = ((int64_t)rb * p.q_len + qi) * p.Hq + g * p.G + hh;   // q / out row
     if (tid < PF_SM_THREADS) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            reinterpret_cast<const T *>(p.q) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * PF_D);
+        const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + orow * PF_D);
         uint8_t *qdst = smem + t_of * PF_Q_BYTES + rt * 128;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {                         // 16 chunks of 8 values, 128-byte swizzle
@@ -167,7 +191,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int sb = lane >> 1, h = lane & 1;
         const bool copier = lane < 2 * PF_SUB;
         auto lookup = [&](int j) -> int {
-            const int tok = j * PF_BN + sb * TILE_TOKENS;
+            const int tok = key0 + j * PF_BN + sb * TILE_TOKENS;
             return (copier && tok < L) ? __ldg(p.block_tables + (int64_t)b * p.stride + tok / p.bs) : 0;
         };
         int id_next = ntiles > 0 ? lookup(0) : 0;
@@ -184,7 +208,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             int id = id_next;
             if (j + 1 < ntiles) id_next = lookup(j + 1);
-            const int rem = L - j * PF_BN;                     // > 0 for every tile issued
+            const int rem = L - key0 - j * PF_BN;              // > 0 for every tile issued
             const int nsub = rem >= PF_BN ? PF_SUB : (rem + TILE_TOKENS - 1) / TILE_TOKENS;
             const uint32_t bar = full0 + st * 8;
             if (lane == 0) mbar_arrive_expect_tx(bar, nsub * 2 * TILE_TOKENS * 128);
@@ -194,7 +218,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     set_status(p.status, STATUS_BOUNDS);
                     id = 0;
                 }
-                const int tok = j * PF_BN + sb * TILE_TOKENS;
+                const int tok = key0 + j * PF_BN + sb * TILE_TOKENS;
                 const int row0 = (id * p.Hkv + g) * p.bs + tok % p.bs;
                 tma_load_2d(ring + st * PF_KV_BYTES + h * PF_HALF_BYTES + sb * TILE_TOKENS * 128, map, h * 64, row0,
                             bar, policy);
@@ -245,7 +269,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const int st = j % PF_VSTAGES;
             if (!wait_lane0(bar_v_full + st * 8, (uint32_t)(j / PF_VSTAGES) & 1u)) return false;
             consumed_v = j + 1;
-            const int t0 = j * PF_BN;
+            const int t0 = key0 + j * PF_BN;
             if (t0 + PF_BN > L) {
                 const int nvalid = L - t0 > 0 ? L - t0 : 0;
                 const int nz = (PF_BN - nvalid) * 8;           // 16-byte chunks per half
@@ -301,7 +325,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int nt = t ? nt1 : nt0;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tmem_s = tmem + t * 256 + lane_base, tmem_o = tmem_s + 128;
-        const int lim = L - p.q_len + qi;                      // last key this row may see
+        // last key this row may see (a cascade row follows the whole prefix)
+        const int lim = CASCADE ? 0x7fffffff : L - p.q_len + qi;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
@@ -312,7 +337,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             tmem_ld_cols(tmem_s, sv);
             // raw-score max (the scale is positive, so it commutes with the max); eight independent
             // partial maxima and sums keep the dependent chains short
-            const int t0 = j * PF_BN;
+            const int t0 = key0 + j * PF_BN;
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
@@ -381,10 +406,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_o_done + t * 8, 0u, p.wait_ns));
         if (!ok) {
             if (lane == 0) *abort_flag = 1;
+        } else if (nt > 0 && CASCADE) {
+            // unnormalised state of the chunk's keys in its first partition slot; the chunk's other
+            // slots are written empty (sum 0, zero O) so that the merge gives them no weight
+            tc_fence_after();
+            const int slot0 = key0 / p.part_tokens, slot1 = L / p.part_tokens;
+            const int64_t prow = orow * p.max_parts + slot0;
+            float *dst = p.part_o + prow * PF_D;
+#pragma unroll
+            for (int c0 = 0; c0 < PF_D; c0 += 32) {
+                float a[32];
+                tmem_ld32(tmem_o + c0, a);
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
+                }
+            }
+            if (row_ok) {
+                p.part_ml[prow] = make_float2(m_ref, l);
+                for (int sl = slot0 + 1; sl < slot1; ++sl) {
+                    float4 *z = reinterpret_cast<float4 *>(p.part_o + (orow * p.max_parts + sl) * PF_D);
+#pragma unroll 4
+                    for (int c = 0; c < PF_D / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    p.part_ml[orow * p.max_parts + sl] = make_float2(0.f, 0.f);
+                }
+            }
         } else if (nt > 0) {
             tc_fence_after();
             const float inv = 1.f / l;
-            T *dst = reinterpret_cast<T *>(p.out) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * PF_D;
+            T *dst = reinterpret_cast<T *>(p.out) + orow * PF_D;
 #pragma unroll
             for (int c0 = 0; c0 < PF_D; c0 += 32) {
                 float a[32];
@@ -424,21 +475,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
 }
 
-template <typename T>
+template <typename T, bool CASCADE>
 static cudaError_t launch_prefill_t(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                     cudaStream_t stream) {
-    const int mtiles = (p.rows + PF_BM - 1) / PF_BM;
-    const int64_t grid = (int64_t)p.num_seqs * p.Hkv * ((mtiles + PF_QT - 1) / PF_QT);
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+    const int64_t rows = CASCADE ? (int64_t)p.num_seqs * p.rows : p.rows;
+    const int64_t ctiles = ((rows + PF_BM - 1) / PF_BM + PF_QT - 1) / PF_QT;
+    const int64_t units = CASCADE ? (int64_t)(p.part0 + p.pchunk - 1) / p.pchunk : (int64_t)p.num_seqs;
+    const int64_t grid = units * p.Hkv * ctiles;
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<T, CASCADE>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
     if (e != cudaSuccess) return e;
-    prefill_kernel<T><<<(unsigned)grid, PF_THREADS, PF_SMEM, stream>>>(tmk, tmv, p);
+    prefill_kernel<T, CASCADE><<<(unsigned)grid, PF_THREADS, PF_SMEM, stream>>>(tmk, tmv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            cudaStream_t stream) {
-    return dtype == PA_FP16 ? launch_prefill_t<__half>(p, tmk, tmv, stream)
-                            : launch_prefill_t<__nv_bfloat16>(p, tmk, tmv, stream);
+    return dtype == PA_FP16 ? launch_prefill_t<__half, false>(p, tmk, tmv, stream)
+                            : launch_prefill_t<__nv_bfloat16, false>(p, tmk, tmv, stream);
+}
+
+cudaError_t launch_prefix(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                          cudaStream_t stream) {
+    return dtype == PA_FP16 ? launch_prefill_t<__half, true>(p, tmk, tmv, stream)
+                            : launch_prefill_t<__nv_bfloat16, true>(p, tmk, tmv, stream);
 }
 
 }  // namespace pa

@@ -58,6 +58,7 @@ def lib() -> C.CDLL:
             L.pa_cache_write.argtypes = [P, P, P, P, I32, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
             L.pa_prefill.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P]
+            L.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, I32, P, P]
             L.pa_pool_check.argtypes = [P, P]
             L.pa_pool_selftest_wait.argtypes = [P, C.c_uint64, P]
             L.pa_pool_selftest_wait.restype = C.c_int
@@ -65,7 +66,8 @@ def lib() -> C.CDLL:
             L.pa_decode_launches.restype = I32
             L.pa_status_string.argtypes = [C.c_int]
             L.pa_status_string.restype = C.c_char_p
-            for f in ("pa_pool_create", "pa_pool_caches", "pa_cache_write", "pa_decode", "pa_prefill", "pa_pool_check"):
+            for f in ("pa_pool_create", "pa_pool_caches", "pa_cache_write", "pa_decode", "pa_prefill", "pa_decode_shared_prefix",
+                      "pa_pool_check"):
                 getattr(L, f).restype = C.c_int
             _lib = L
     return _lib
@@ -172,6 +174,24 @@ class Pool:
         _check(lib().pa_decode(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
                                _stream(stream)), "pa_decode")
+        return out
+
+    def decode_shared_prefix(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             scale: float, prefix_tokens: int, out: Optional[torch.Tensor] = None,
+                             k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """pa_decode_shared_prefix: decode for sequences whose tables share their first prefix_tokens tokens."""
+        _dev(q, "q", self.dtype)
+        _dev(block_tables, "block_tables", torch.int32)
+        _dev(context_lens, "context_lens", torch.int32)
+        B, q_len, Hq, d = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        _dev(out, "out", self.dtype)
+        _check(lib().pa_decode_shared_prefix(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                             block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale),
+                                             int(prefix_tokens), _ptr(out), _stream(stream)),
+               "pa_decode_shared_prefix")
         return out
 
     def prefill(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,

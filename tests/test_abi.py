@@ -57,6 +57,8 @@ def test_host_validation_without_gpu(lib):
     L = lib.lib()
     assert L.pa_decode(None, None, None, None, None, 1, None, 1, 8, 1, 0.1, None, None) == lib.PA_ERR_INVALID_ARG
     assert L.pa_prefill(None, None, None, None, None, 1, None, 1, 8, 16, 0.1, None, None) == lib.PA_ERR_INVALID_ARG
+    assert L.pa_decode_shared_prefix(None, None, None, None, None, 1, None, 1, 8, 1, 0.1, 512, None,
+                                     None) == lib.PA_ERR_INVALID_ARG
     assert L.pa_cache_write(None, None, None, None, 1, None, None, None) == lib.PA_ERR_INVALID_ARG
     assert L.pa_pool_check(None, None) == lib.PA_ERR_INVALID_ARG
     L.pa_destroy(None)
