@@ -35,24 +35,24 @@
 namespace pa {
 
 // Pipeline depth per warp and resident CTAs per SM: 16-bit stages are 8 KB (3 stages, 2 CTAs per
-// SM); FP8 stages are 4 KB, so 2 stages leave room for 4 single-column-tile CTAs per SM (16 warps)
-// to hide the per-tile conversion latency.
+// SM); FP8 stages are 4 KB (3 stages), with 4 single-column-tile CTAs per SM (16 warps) to hide the
+// latency of each tile's code conversions.
 #ifndef PA_FP8_STAGES
-#define PA_FP8_STAGES 2
+#define PA_FP8_STAGES 3
 #endif
 __host__ __device__ constexpr int stages_for(bool kv8) { return kv8 ? PA_FP8_STAGES : 3; }
-__host__ __device__ constexpr int min_ctas_for(bool kv8, int nt) { return kv8 && nt == 1 && PA_FP8_STAGES == 2 ? 4 : 2; }
+__host__ __device__ constexpr int min_ctas_for(bool kv8, int nt) { return kv8 && nt == 1 ? 4 : 2; }
 
 // Shared memory of the tile pipelines. 16-bit pools: each stage holds the K tile then the V tile
 // (16 rows x D 16-bit values each). FP8 pools (D = 128): each stage holds the K codes tile and the V
 // codes tile (16 rows x 128 bytes each, 1024-byte aligned for the 128-byte swizzle); the stages'
-// K and V scales (16 floats each) sit in a small region after all code tiles; then each warp owns
-// one 16-bit tile that it converts K codes into for the scores and then V codes into for P.V.
+// K and V scales (16 floats each) sit in a small region after all code tiles. The codes are
+// converted to fp16 in registers, on their way from ldmatrix to the MMAs.
 __host__ __device__ constexpr int stage_bytes(int D, bool kv8) { return kv8 ? 2 * TILE_TOKENS * 128 : 2 * TILE_TOKENS * D * 2; }
 __host__ __device__ constexpr int scale_region(bool kv8) { return kv8 ? DECODE_WARPS * stages_for(kv8) * 2 * TILE_TOKENS * 4 : 0; }
 __host__ __device__ constexpr int ring_bytes(int D, bool kv8) {
     return DECODE_WARPS * stages_for(kv8) * stage_bytes(D, kv8) +
-           (kv8 ? ((scale_region(kv8) + 1023) & ~1023) + DECODE_WARPS * TILE_TOKENS * D * 2 : 0);
+           (kv8 ? ((scale_region(kv8) + 1023) & ~1023) : 0);
 }
 __host__ __device__ constexpr int merge_bytes(int D, int nt) {
     return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4;
@@ -67,27 +67,6 @@ static size_t smem_bytes(int D, int nt, bool kv8, int table_entries) {
 }
 
 size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt, false, 0); }
-
-// E4M3 codes of one 16 x 128 tile (128-byte rows, 128-byte swizzle) -> the fp16 tile layout of a
-// 16-bit stage (two 64-value halves of 16 x 128 bytes, same swizzle). Lane l converts row l/2,
-// half l%2; codes are exact in fp16.
-__device__ __forceinline__ void convert_codes(const uint8_t *codes, uint8_t *tile, int lane) {
-    const int r = lane >> 1, h = lane & 1;
-    const uint8_t *src = codes + r * 128;
-    uint8_t *dst = tile + h * (TILE_TOKENS * 128) + r * 128;
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c = 4 * h + cc;                                   // 16-code chunk: dims 16c..16c+15
-        const uint4 raw = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
-        const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t outw[8];
-#pragma unroll
-        for (int q2 = 0; q2 < 8; ++q2) outw[q2] = e4m3x2_to<__half>((uint16_t)(wds[q2 >> 1] >> ((q2 & 1) * 16)));
-        const int c16 = 2 * cc;                                     // 8-value chunks within the half
-        *reinterpret_cast<uint4 *>(dst + ((c16 ^ (r & 7)) << 4)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        *reinterpret_cast<uint4 *>(dst + (((c16 + 1) ^ (r & 7)) << 4)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-    }
-}
 
 template <typename T, int D, int NT, bool KV8>
 __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
@@ -166,7 +145,6 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     const int my_tiles = ntiles > warp ? (ntiles - warp + DECODE_WARPS - 1) / DECODE_WARPS : 0;
     const uint32_t ring_u32 = base_u32 + warp * STAGES * STAGE_BYTES;
     const uint32_t scales_u32 = base_u32 + DECODE_WARPS * STAGES * STAGE_BYTES;                 // FP8 only
-    const uint32_t conv_u32 = scales_u32 + ((scale_region(KV8) + 1023) & ~1023) + warp * TILE_BYTES;   // FP8 only
     const uint64_t policy = l2_policy_evict_first();
 
     auto issue = [&](int it) {
@@ -214,8 +192,10 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
                 reinterpret_cast<const T *>(p.q) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * D);
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                qf[nt][ks][0] = __ldg(qrow + ks * 8 + tq);
-                qf[nt][ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
+                // FP8 pools: the K codes reach the MMA with each lane holding 4 consecutive dims
+                // (16 ks + 4 tq ..), so the contraction index is permuted the same way for Q
+                qf[nt][ks][0] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq : tq));
+                qf[nt][ks][1] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq + 1 : 4 + tq));
                 if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -266,20 +246,16 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
         uint32_t vb = kb + TILE_BYTES;
         float ks_lo = 1.f, ks_hi = 1.f, vs_lo = 1.f, vs_hi = 1.f;   // FP8: scales of this thread's key rows
         if constexpr (KV8) {
-            // Convert the tile's K codes into this warp's fp16 tile (same swizzled layout as a 16-bit
-            // stage; codes are exact in fp16). The K scale multiplies the scores and the V scale
-            // multiplies P; the V codes are converted into the same tile after the scores.
+            // K and V codes enter the MMAs straight from the stage (exact in fp16). The K scale
+            // multiplies the scores and the V scale multiplies P.
             const float *sk = reinterpret_cast<const float *>(smem + (scales_u32 - base_u32)) +
                               (warp * STAGES + s) * 2 * TILE_TOKENS;
             const float *sv = sk + TILE_TOKENS;
-            convert_codes(smem + (kb - base_u32), smem + (conv_u32 - base_u32), lane);
             ks_lo = sk[gq_] * p.scale_log2;
             ks_hi = sk[gq_ + 8] * p.scale_log2;
             vs_lo = sv[gq_];
             vs_hi = sv[gq_ + 8];
-            __syncwarp();
-            vb = kb + CODE_BYTES;                         // V codes stay in the stage until converted
-            kb = conv_u32;
+            vb = kb + CODE_BYTES;
         }
 
         // Rows past the context hold other data (possibly NaN): zero them in V so that
@@ -300,7 +276,29 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
         float sacc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-        {
+        if constexpr (KV8) {
+            // ldmatrix.x4 on the codes viewed as 16-bit pairs: matrices (keys 0-7 | 8-15) x (chunk
+            // 2kp | 2kp+1), each lane receiving 4 consecutive codes (dims 16c + 4tq ..) of key gq or
+            // gq + 8. Codes 0-1 / 2-3 are the A fragment's k pairs (2tq) / (2tq + 8) of the permuted
+            // contraction index.
+            const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int kp = 0; kp < KSTEPS / 2; ++kp) {
+                const int chunk = kp * 2 + (lane >> 4);
+                const uint32_t addr = kb + krow * 128 + ((chunk ^ (krow & 7)) << 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(addr, r0, r1, r2, r3);
+                const uint32_t a0 = e4m3x2_to<__half>((uint16_t)r0), a2 = e4m3x2_to<__half>((uint16_t)(r0 >> 16));
+                const uint32_t a1 = e4m3x2_to<__half>((uint16_t)r1), a3 = e4m3x2_to<__half>((uint16_t)(r1 >> 16));
+                const uint32_t c0 = e4m3x2_to<__half>((uint16_t)r2), c2 = e4m3x2_to<__half>((uint16_t)(r2 >> 16));
+                const uint32_t c1 = e4m3x2_to<__half>((uint16_t)r3), c3 = e4m3x2_to<__half>((uint16_t)(r3 >> 16));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816<M>(sacc[nt], a0, a1, a2, a3, qf[nt][2 * kp][0], qf[nt][2 * kp][1]);
+                    mma_16816<M>(sacc[nt], c0, c1, c2, c3, qf[nt][2 * kp + 1][0], qf[nt][2 * kp + 1][1]);
+                }
+            }
+        } else {
             const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -373,28 +371,40 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
         }
 
         if constexpr (KV8) {
-            __syncwarp();                                 // every lane's K ldmatrix reads are done
-            convert_codes(smem + (vb - base_u32), smem + (conv_u32 - base_u32), lane);
-            if (nvalid < TILE_TOKENS) {                   // rows past the context: zero (codes may be NaN)
-                const int nz = (TILE_TOKENS - nvalid) * 8;
-                uint8_t *vgen = smem + (conv_u32 - base_u32);
-                for (int c = lane; c < nz * HALVES; c += 32) {
-                    const int h = c / nz, rc = c - (c / nz) * nz;
-                    *reinterpret_cast<uint4 *>(vgen + h * HALF_BYTES + (nvalid + rc / 8) * 128 + (rc % 8) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
+            if (nvalid < TILE_TOKENS) {                   // V code rows past the context: zero (may be NaN)
+                uint8_t *vgen = smem + (vb - base_u32);
+                for (int c = lane; c < (TILE_TOKENS - nvalid) * 8; c += 32)
+                    *reinterpret_cast<uint4 *>(vgen + (nvalid + c / 8) * 128 + (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                __syncwarp();
             }
-            __syncwarp();
-            // the stage's codes and scales are consumed: refill it now
-            if (it + STAGES < my_tiles) {
-                if (lane == 0) issue(it + STAGES);
-                ++issued;
-            }
-            vb = conv_u32;
         }
 
         // O^T += V^T . P^T
-        {
+        if constexpr (KV8) {
+            // ldmatrix.x4.trans on the codes viewed as 16-bit pairs: matrices (keys 0-7 | 8-15) x
+            // (chunk 2mp | 2mp+1); each lane receives keys 2tq, 2tq+1 x dims 2gq, 2gq+1 of the chunk.
+            // Bytes (0, 2) / (1, 3) give the A fragment of V^T whose rows are the chunk's even / odd
+            // dims (row m <-> dim 16 md + 2 (m % 8) + m / 8, undone when O is written).
+            const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int mp = 0; mp < MT / 2; ++mp) {
+                const int chunk = mp * 2 + (lane >> 4);
+                const uint32_t addr = vb + vrow * 128 + ((chunk ^ (vrow & 7)) << 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_trans(addr, r0, r1, r2, r3);
+                const uint32_t rr[4] = {r0, r1, r2, r3};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t lo = rr[2 * h], hi = rr[2 * h + 1];   // keys 0-7 / 8-15 of chunk 2mp + h
+                    const uint32_t a0 = e4m3x2_to<__half>((uint16_t)__byte_perm(lo, 0u, 0x4420));
+                    const uint32_t a1 = e4m3x2_to<__half>((uint16_t)__byte_perm(lo, 0u, 0x4431));
+                    const uint32_t a2 = e4m3x2_to<__half>((uint16_t)__byte_perm(hi, 0u, 0x4420));
+                    const uint32_t a3 = e4m3x2_to<__half>((uint16_t)__byte_perm(hi, 0u, 0x4431));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_16816<M>(o[2 * mp + h][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                }
+            }
+        } else {
             const int vrow = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
             for (int md = 0; md < MT; ++md) {
@@ -410,11 +420,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
             }
         }
         __syncwarp();
-        if constexpr (!KV8) {
-            if (it + STAGES < my_tiles) {
-                if (lane == 0) issue(it + STAGES);
-                ++issued;
-            }
+        if (it + STAGES < my_tiles) {
+            if (lane == 0) issue(it + STAGES);
+            ++issued;
         }
     }
 
@@ -452,7 +460,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int dim = md * 16 + gq + (e >> 1) * 8;
+                // FP8 pools: O's rows are the chunk's even dims, then its odd dims
+                const int dim = KV8 ? md * 16 + 2 * gq + (e >> 1) : md * 16 + gq + (e >> 1) * 8;
                 const int col = nt * 8 + 2 * tq + (e & 1);
                 ow[(warp * RP + col) * OSTR + dim] = o[md][nt][e];
             }
