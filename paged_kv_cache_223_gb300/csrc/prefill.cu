@@ -153,6 +153,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         issued_tiles[1] = 0;
         fence_barrier_init();
     }
+    // barriers and the tensor-memory address are published; the copy warps start at once while the
+    // softmax threads load Q (published to the MMA warp by named barrier 1)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int consumed_k = 0, consumed_v = 0;                        // MMA thread: tiles whose copies landed
     // softmax threads: row tile t = tid / 128, row rt = tid % 128
     const int t_of = tid >> 7, rt = tid & (PF_BM - 1);
     const int r = (ct * PF_QT + t_of) * PF_BM + rt;
@@ -162,21 +169,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int qi = rr / p.G;
     const int hh = rr - qi * p.G;
     const int64_t orow = ((int64_t)rb * p.q_len + qi) * p.Hq + g * p.G + hh;   // q / out row
-    if (tid < PF_SM_THREADS) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + orow * PF_D);
-        uint8_t *qdst = smem + t_of * PF_Q_BYTES + rt * 128;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {                         // 16 chunks of 8 values, 128-byte swizzle
-            const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(qdst + (c >> 3) * (PF_BM * 128) + (((c & 7) ^ (rt & 7)) << 4)) = v;
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    int consumed_k = 0, consumed_v = 0;                        // MMA thread: tiles whose copies landed
+    constexpr uint32_t Q_BARRIER = 1, Q_BARRIER_THREADS = PF_SM_THREADS + 32;   // softmax + MMA warps
 
     if (warp >= PF_PRODUCER_WARP) {
       setmaxnreg_dec<PF_REGS_OTHER>();
@@ -184,7 +177,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         // ---------------------------------------------------------------- K or V producer
         const bool is_v = warp == PF_VPRODUCER_WARP;
         const int nst = is_v ? PF_VSTAGES : PF_KSTAGES;
-        const uint32_t full0 = is_v ? bar_v_full : bar_k_full, empty0 = is_v ? bar_v_empty : bar_k_empty;
+        const uint32_t full0 = is_v ? bar_v_full : bar_k_full;
         const uint32_t ring = base + (is_v ? PF_OFF_V : PF_OFF_K);
         const CUtensorMap *map = is_v ? &tmv : &tmk;
         const uint64_t policy = l2_policy_evict_last();       // re-read by the unit's other row tiles
@@ -198,8 +191,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         int j = 0;
         for (; j < ntiles; ++j) {
             const int st = j % nst;
+            // K(j) reuses the stage of K(j - 3), freed by the commit after S(j - 3). V(j) reuses the
+            // stage of V(j - 2), read by P(j - 2).V, which was issued before S(j - 1): the commit
+            // after S(j - 1) covers it
+            const int rel = is_v ? j - 1 : j - PF_KSTAGES;     // key tile whose release frees the stage
             if (j >= nst) {
-                const bool got = mbar_wait_bounded(empty0 + st * 8, (uint32_t)((j - nst) / nst) & 1u, p.wait_ns);
+                const bool got = mbar_wait_bounded(bar_k_empty + (rel % PF_KSTAGES) * 8,
+                                                   (uint32_t)(rel / PF_KSTAGES) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) {
                     if (lane == 0) *abort_flag = 1;
                     break;
@@ -235,10 +233,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint64_t dk0 = umma_desc_sw128(base + PF_OFF_K, 16, 1024);
         const uint64_t dv0 = umma_desc_sw128(base + PF_OFF_V, PF_HALF_BYTES, 1024);
         bool ok = true;
+        named_barrier_sync(Q_BARRIER, Q_BARRIER_THREADS);      // Q is in shared memory
         auto wait_lane0 = [&](uint32_t bar, uint32_t parity) -> bool {
-            bool got = true;
-            if (lane == 0) got = mbar_wait_bounded(bar, parity, p.wait_ns);
-            return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            return mbar_wait_bounded(bar, parity, p.wait_ns);
         };
         auto issue_pv = [&](int t, int j) {                   // O_t += P_t(j) V(j)
             const uint64_t dv = dv0 + (uint64_t)((j % PF_VSTAGES) * (PF_KV_BYTES >> 4));
@@ -274,16 +271,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const int nvalid = L - t0 > 0 ? L - t0 : 0;
                 const int nz = (PF_BN - nvalid) * 8;           // 16-byte chunks per half
                 uint8_t *vg = smem + PF_OFF_V + st * PF_KV_BYTES;
-                for (int c = lane; c < 2 * nz; c += 32) {
+                for (int c = 0; c < 2 * nz; ++c) {
                     const int hf = c / nz, rc = c - hf * nz;
                     *reinterpret_cast<uint4 *>(vg + hf * PF_HALF_BYTES + (nvalid + rc / 8) * 128 + (rc % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                __syncwarp();
             }
             return true;
         };
+        if (lane == 0) {                                       // one thread issues; the warp's other lanes idle
         for (int j = 0; j < ntiles && ok; ++j) {
             if (!(ok = wait_lane0(bar_k_full + (j % PF_KSTAGES) * 8, (uint32_t)(j / PF_KSTAGES) & 1u))) break;
             consumed_k = j + 1;
@@ -298,10 +295,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 if (lane == 0) issue_pv(1, j - 1);
             }
             if (j < nt1 && lane == 0) issue_s(1, j);
-            if (lane == 0) {
-                umma_commit(bar_k_empty + (j % PF_KSTAGES) * 8);
-                if (j > 0) umma_commit(bar_v_empty + ((j - 1) % PF_VSTAGES) * 8);
-            }
+            umma_commit(bar_k_empty + (j % PF_KSTAGES) * 8);   // frees K(j), and V(j - 1) after P(j-1).V
         }
         if (ok && ntiles > 0) {
             ok = v_ready(ntiles - 1);
@@ -313,13 +307,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 ok = wait_lane0(bar_p_full + 8, (uint32_t)(ntiles - 1) & 1u);
                 if (ok && lane == 0) issue_pv(1, ntiles - 1);
             }
-            if (ok && lane == 0)
+            if (ok)
                 for (int t = 0; t < PF_QT; ++t) umma_commit(bar_o_done + t * 8);
         }
-        if (!ok && lane == 0) *abort_flag = 1;
+        }
+        __syncwarp();
+        if (!ok) *abort_flag = 1;
       }
     } else {
         setmaxnreg_inc<PF_REGS_SOFTMAX>();
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + orow * PF_D);
+            uint8_t *qdst = smem + t_of * PF_Q_BYTES + rt * 128;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {                     // 16 chunks of 8 values, 128-byte swizzle
+                const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(qdst + (c >> 3) * (PF_BM * 128) + (((c & 7) ^ (rt & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(Q_BARRIER, Q_BARRIER_THREADS);
+        }
         // ---------------------------------------------------------------- softmax (row tile t_of)
         const int t = t_of;
         const int nt = t ? nt1 : nt0;

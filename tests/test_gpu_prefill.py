@@ -91,3 +91,38 @@ def test_prefill_deterministic_and_rejects():
     n = torch.full((1,), 4, dtype=torch.int32, device=H.DEV)
     with pytest.raises(RuntimeError):
         small.prefill(q64, t, n, 0.125)
+
+
+@pytest.mark.parametrize("dt", [synth.FP16, synth.BF16], ids=["fp16", "bf16"])
+def test_prefill_benchmark_workload_sampled(dt):
+    """The benchmark's prefill pool at full size (8 sequences, 512-token chunk ending at context 4608, Hq 64,
+    Hkv 8), launched as the benchmark launches it; the oracle checks the first and last sequences."""
+    wl = synth.custom_workload([4608] * 8, 64, 8, 128, 16, 512, dt, tag=500)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    out = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    seqs = [0, wl.B - 1]
+    ref, hk, hv = H.oracle_reference(wl, 0, seqs)
+    H.check_pool_blocks(wl, 0, kc, vc, hk, hv, seqs)
+    H.assert_close(out[seqs], ref, "prefill benchmark workload")
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("case", [([2048], 8, 2, 16, 2048, synth.FP16),      # a 2048-token first chunk
+                                  ([1536, 3000], 16, 4, 32, 1024, synth.BF16)],  # 1024-token chunks, bs 32
+                         ids=["chunk2048", "chunk1024_bs32"])
+def test_prefill_long_chunks(case):
+    lens, Hq, Hkv, bs, C, dt = case
+    wl = synth.custom_workload(lens, Hq, Hkv, 128, bs, C, dt, tag=330 + C // 512)
+    pool, kc, vc, q, tables, lens_d = H.build_device(wl)
+    out = pool.prefill(q, tables, lens_d, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _, _ = H.oracle_reference(wl, 0)
+    H.assert_close(out, ref, f"prefill {case}")
+
+
+def test_prefill_rejects_fp8_pools():
+    wl = synth.custom_workload([64], 8, 2, 128, 16, 16, synth.FP16, tag=331)
+    pool, kc, vc, q, tables, lens = H.build_device(wl, kv_format=pa.PA_KV_FP8_E4M3)
+    with pytest.raises(RuntimeError):
+        pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
