@@ -535,8 +535,9 @@ __host__ __device__ inline int merge_threads(int pairs, int max_parts) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams p) {
-    extern __shared__ float msm[];                 // weights [G][max_parts], den [G], sums [groups][G*D]
-    const int unit = blockIdx.x;                   // (b, qi, g)
+    extern __shared__ float msm[];                 // weights [G][max_parts], den [G], sums [groups][pairs]
+    const int unit = blockIdx.x / p.merge_splits;  // (b, qi, g)
+    const int split = blockIdx.x - unit * p.merge_splits;
     const int g = unit % p.Hkv;
     const int bq = unit / p.Hkv;                   // b * q_len + qi
     const int b = bq / p.q_len;
@@ -575,10 +576,15 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
     }
     __syncthreads();
 
-    const int pairs = G * (D / 4);
-    const int groups = merge_groups(pairs, p.max_parts);
+    // this CTA's share of the unit's (row, 4 dims) pairs
+    const int all_pairs = G * (D / 4);
+    const int pps = (all_pairs + p.merge_splits - 1) / p.merge_splits;
+    const int pair0 = split * pps;
+    const int pairs = min(pps, all_pairs - pair0);
+    if (pairs <= 0) return;
+    const int groups = merge_groups(pps, p.max_parts);
     for (int t = threadIdx.x; t < pairs * groups; t += nthreads) {
-        const int pair = t % pairs;
+        const int pair = pair0 + t % pairs;
         const int grp = t / pairs;
         const int r = pair / (D / 4);
         const int d4 = pair - r * (D / 4);
@@ -594,13 +600,14 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
             acc.z += c * x.z;
             acc.w += c * x.w;
         }
-        sums[grp * pairs + pair] = acc;
+        sums[grp * pairs + (pair - pair0)] = acc;
     }
     __syncthreads();
-    for (int q = threadIdx.x; q < pairs; q += nthreads) {
-        float4 t = sums[q];
+    for (int q0 = threadIdx.x; q0 < pairs; q0 += nthreads) {
+        const int q = pair0 + q0;
+        float4 t = sums[q0];
         for (int k = 1; k < groups; ++k) {
-            const float4 u = sums[k * pairs + q];
+            const float4 u = sums[k * pairs + q0];
             t.x += u.x;
             t.y += u.y;
             t.z += u.z;
@@ -658,16 +665,27 @@ cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const 
     return cudaErrorInvalidValue;
 }
 
-size_t merge_smem_bytes(int G, int max_parts, int head_dim) {
-    const int pairs = G * (head_dim / 4);
+size_t merge_smem_bytes(int G, int max_parts, int head_dim, int splits) {
+    const int pps = (G * (head_dim / 4) + splits - 1) / splits;
     return (size_t)(merge_wt_floats(G, max_parts) + merge_den_floats(G)) * sizeof(float) +
-           (size_t)merge_groups(pairs, max_parts) * pairs * sizeof(float4);
+           (size_t)merge_groups(pps, max_parts) * pps * sizeof(float4);
+}
+
+// Merge CTAs per unit: enough for about two CTAs per SM, each keeping at least 8 (row, 4-dim) pairs.
+int merge_splits_for(int64_t units, int G, int head_dim, int sm_count) {
+    const int pairs = G * (head_dim / 4);
+    if (units <= 0 || sm_count <= 0) return 1;
+    int64_t want = (2LL * sm_count + units - 1) / units;
+    const int cap = pairs / 8 > 0 ? pairs / 8 : 1;
+    if (want > cap) want = cap;
+    return want < 1 ? 1 : (int)want;
 }
 
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
-    const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv;
-    const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim);
-    const int threads = merge_threads(p.G * (head_dim / 4), p.max_parts);
+    const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv * p.merge_splits;
+    const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim, p.merge_splits);
+    const int pps = (p.G * (head_dim / 4) + p.merge_splits - 1) / p.merge_splits;
+    const int threads = merge_threads(pps, p.max_parts);
     cudaError_t e = cudaSuccess;
 #define PA_MERGE(TT, DD)                                                                                       \
     e = cudaFuncSetAttribute(merge_kernel<TT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \

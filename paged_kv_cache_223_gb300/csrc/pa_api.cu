@@ -313,6 +313,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     if ((st = tensor_map(pool, k_cache, &tmk)) != PA_OK) return st;
     if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, pool->cfg.head_dim, pool->sm_count);
     if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s, kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
@@ -376,6 +377,7 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
     if (launch_decode(p, c.dtype, c.head_dim, tmk, tmv, s, false) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaEventRecord(pool->ev_join, pool->side) != cudaSuccess || cudaStreamWaitEvent(s, pool->ev_join, 0) != cudaSuccess)
         return PA_ERR_CUDA;
+    p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, c.head_dim, pool->sm_count);
     if (launch_merge(p, c.dtype, c.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }

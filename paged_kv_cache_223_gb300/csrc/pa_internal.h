@@ -44,6 +44,8 @@ struct DecodeParams {
     int part0 = 0;       // shared-prefix decode: partitions below part0 (the prefix) come from the prefix
                          // kernel; the decode covers [part0, max_parts)
     int pchunk = 1;      // prefix partitions per prefix-kernel CTA (their combined state goes to the first)
+    int merge_splits = 1;  // merge CTAs per (sequence, query position, KV head): each takes a share of
+                           // the (row, 4-dim) columns, so small batches still fill the GPU
 };
 
 struct CacheWriteParams {
@@ -83,7 +85,8 @@ cudaError_t launch_prefix(const DecodeParams &p, int dtype, const CUtensorMap &t
                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int nt);
 size_t prefill_smem_bytes();
-size_t merge_smem_bytes(int G, int max_parts, int head_dim);
+size_t merge_smem_bytes(int G, int max_parts, int head_dim, int splits = 1);
+int merge_splits_for(int64_t units, int G, int head_dim, int sm_count);
 constexpr size_t MAX_SMEM_PER_CTA = 227 * 1024;
 
 }  // namespace pa
