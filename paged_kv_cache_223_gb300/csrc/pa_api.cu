@@ -274,11 +274,23 @@ static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_
     return PA_OK;
 }
 
+// When the (sequence, KV head) units alone fill several waves of CTAs and a context spans only a few
+// partitions, splitting buys no parallelism and costs the partials and the merge launch: decode each
+// context as one partition.
+static void unsplit_if_filled(const pa_pool *pool, DecodeParams &p) {
+    const int64_t units = (int64_t)p.num_seqs * p.Hkv;
+    if (p.max_parts > 1 && p.max_parts <= 4 && units >= 6LL * pool->sm_count) {
+        p.part_tokens = p.max_parts * p.part_tokens;
+        p.max_parts = 1;
+    }
+}
+
 int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int32_t num_seqs, int32_t num_q_heads,
                            int32_t q_len) {
     if (!pool) return -1;
     DecodeParams p;
     if (decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p) != PA_OK) return -1;
+    unsplit_if_filled(pool, p);
     return p.max_parts > 1 ? 2 : 1;
 }
 
@@ -297,6 +309,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     DecodeParams p;
     pa_status st = decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p);
     if (st != PA_OK) return st;
+    unsplit_if_filled(pool, p);
     p.q = q;
     p.out = out;
     p.block_tables = block_tables;
