@@ -10,6 +10,8 @@ KV, far larger than L2, so no flush is needed between steps).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3|cfg5|cfg2|cfg4|cfg1]
     python bench.py --impl reference      # the fp64 CPU oracle as the reference arm
     python bench.py --workload prefill    # chunked prefill (pa_prefill), tensor-core bound: TFLOP/s
+    python bench.py --workload cow        # copy-on-write block copies (pa_copy_blocks): GB/s
+    python bench.py --workload spec       # speculative rejection sampling (pa_spec_verify): GB/s
 
 Under torchrun each rank runs the same workload on its own GPU (weak scaling, no collective
 on the data path); the time is the maximum over ranks.
@@ -33,7 +35,7 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 import synth  # noqa: E402
 
-WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "prefill": 0}
+WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "prefill": 0, "cow": -1, "spec": -2}
 DESCR = {
     1: "tiny paged decode (B4, lens 17/64/100/200, Hq8 Hkv2 d64 bs16, fp16)",
     2: "Llama-3-8B-shaped decode layer (B64, lens U[512,4096], Hq32 Hkv8 d128 bs16, bf16)",
@@ -44,6 +46,12 @@ DESCR = {
        "context 4608 (the 9th chunk of the prompt), Hq64 Hkv8 d128 bs16, 8 layer pools",
 }
 PREFILL = dict(batch=8, chunk=512, context=4608, layers=8)
+DESCR[-1] = ("copy-on-write block copies in a Llama-3-70B-shaped layer pool (32768 blocks of 16 tokens, Hkv 8, "
+             "d 128, fp16): 4096 shared blocks copied to private ones, K and V")
+DESCR[-2] = ("speculative rejection sampling: 128 sequences x 5 drafts over a 128256-token vocabulary (fp32 "
+             "target and draft distributions, seeded)")
+COW = dict(num_blocks=32768, Hkv=8, bs=16, d=128, pairs=4096)
+SPEC = dict(B=128, K=5, V=128256)
 
 
 def dist_env():
@@ -514,6 +522,224 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------------------------- CoW copy, spec verify
+
+def _timed(fn, steps: int, warmup: int, dev, events_per_step: bool = True):
+    """CUDA-event time of `steps` calls (after `warmup`); returns (elapsed ms, per-call ms list, clocks)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(steps):
+            evs[i][0].record()
+            fn()
+            evs[i][1].record()
+        stop.record()
+        torch.cuda.synchronize()
+    return start.elapsed_time(stop), [a.elapsed_time(b) for a, b in evs], clk.summary()
+
+
+def _timed_graph(fn, steps: int, warmup: int, dev, calls: int = 16):
+    """`calls` calls of fn captured once in a CUDA graph (as a serving loop issues them, with no host work
+    between launches); CUDA-event time of `steps` replays after `warmup`. Returns (elapsed ms over all
+    replays, per-call ms list (one entry per replay), clocks)."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()                                            # first call outside capture (binding set-up)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    elapsed, per, clocks = _timed(g.replay, steps, warmup, dev)
+    return elapsed, [x / calls for x in per], clocks
+
+
+def cow_pairs():
+    """4096 (shared source, private destination) block pairs from a seeded permutation of the pool."""
+    perm = synth.permutation(0x5EED0100, synth.make_stream(100, 0, 0), COW["num_blocks"])
+    n = COW["pairs"]
+    return np.stack([perm[:n], perm[n:2 * n]], axis=1).astype(np.int32)
+
+
+def run_cow(args):
+    import torch
+    from paged_kv_cache_223_gb300 import pagedattn as pa
+    import synth.device as sdev
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    c = COW
+    pool = pa.Pool(c["num_blocks"], c["bs"], c["Hkv"], c["d"], torch.float16, 0, max_seqs=1, max_q_heads=c["Hkv"],
+                   max_q_len=1, max_context_len=c["bs"])
+    for t in (pool.k_cache, pool.v_cache):
+        sdev.fill_word(t, 0x3C00)                       # any defined content: the copy moves raw words
+    pairs_h = cow_pairs()
+    pairs = torch.from_numpy(pairs_h).to(dev)
+    block_bytes = c["Hkv"] * c["bs"] * c["d"] * 2
+    nbytes = 2 * len(pairs_h) * 2 * block_bytes          # K and V, read + write
+    elapsed, per, clocks = _timed(lambda: pa.copy_blocks(pool, pairs), args.steps, args.warmup, dev)
+    assert pool.check() == 0
+    # end to end: pairs from pinned host memory, the copy, one destination block read back
+    host_pairs = torch.from_numpy(pairs_h).pin_memory()
+    back = torch.empty((c["Hkv"], c["bs"], c["d"]), dtype=torch.float16).pin_memory()
+    dst0 = int(pairs_h[0, 1])
+
+    def one():
+        pairs.copy_(host_pairs, non_blocking=True)
+        pa.copy_blocks(pool, pairs)
+        back.copy_(pool.k_cache[dst0], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    one()
+    n = max(3, args.steps // 5)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t0) / n
+    peak, peak_kind = peaks()
+    call = float(np.mean(per))
+    line = {"metric": "copy-on-write block copy GB/s on 1 GB300 (fraction of HBM peak)",
+            "value": round(nbytes * args.steps / (elapsed * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 words (raw copy)",
+            "data": "synthetic", "config": {"workload": "cow: " + DESCR[-1], **c,
+                                            "l2": "2 x 512 MB moved per step (no flush)"},
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (call * 1e-3) / 1e9, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                         "kernel": "pa_copy_blocks call", "algorithmic_bytes_per_launch": nbytes,
+                         "avg_launch_ms": round(call, 5), "peak_kind": peak_kind},
+            "e2e": {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(pairs_h.nbytes),
+                    "d2h_bytes_per_step": block_bytes, "ms_per_step": round(dt * 1e3, 3), "steps": n},
+            "gpu_launches": args.steps, "clocks": clocks}
+    if not args.no_cpu_baseline:
+        import oracle
+        shape = (c["num_blocks"], c["Hkv"], c["bs"], c["d"])
+        hk = np.zeros(shape, dtype=np.uint16)
+        hv = np.zeros(shape, dtype=np.uint16)
+        t0 = time.perf_counter()
+        reps = 0
+        while reps == 0 or time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            oracle.copy_blocks(hk, hv, pairs_h)
+            reps += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(reps * nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": f"{reps} passes over the 4096 pairs in {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def spec_inputs(dev):
+    """Seeded target/draft distributions (sharpened uniforms, normalised), drafts drawn from the draft
+    distributions by inverse CDF, and the uniforms of the accept tests and of the resample."""
+    import torch
+    c = SPEC
+    g = torch.Generator(device=dev)
+    g.manual_seed(0x5EED0200)
+    def dist(*shape):
+        x = torch.rand(*shape, generator=g, device=dev) ** 3
+        return x / x.sum(-1, keepdim=True)
+    p = dist(c["B"], c["K"] + 1, c["V"])
+    q = dist(c["B"], c["K"], c["V"])
+    # mix part of the target into the draft so that some drafts are accepted
+    q = 0.5 * q + 0.5 * p[:, :c["K"]]
+    q = q / q.sum(-1, keepdim=True)
+    r = torch.rand(c["B"], c["K"], 1, generator=g, device=dev, dtype=torch.float64)
+    draft = torch.searchsorted(torch.cumsum(q.double(), -1), r * q.double().sum(-1, keepdim=True)).squeeze(-1)
+    draft = draft.clamp_(max=c["V"] - 1).to(torch.int32)
+    u = torch.rand(c["B"], c["K"], generator=g, device=dev)
+    v = torch.rand(c["B"], generator=g, device=dev)
+    return p.contiguous(), q.contiguous(), draft.contiguous(), u, v
+
+
+def spec_bytes(n_out: np.ndarray, K: int, V: int) -> int:
+    """Bytes a call must move: per sequence the K draft ids, uniforms and the two probabilities of each accept
+    test, the rows of the resample (p and q of the rejected position, or p of the bonus position), v, and the
+    K+1 output ids and the count."""
+    total = 0
+    for n in n_out.tolist():
+        kept = n - 1
+        tests = min(kept + 1, K)
+        rows = 2 if kept < K else 1
+        total += 4 * K + 4 * K + 8 * tests + rows * 4 * V + 4 + 4 * (K + 1) + 4
+    return total
+
+
+def run_spec(args):
+    import torch
+    from paged_kv_cache_223_gb300 import pagedattn as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    c = SPEC
+    p, q, draft, u, v = spec_inputs(dev)
+    out, n_out = pa.spec_verify(p, q, draft, u, v)
+    torch.cuda.synchronize()
+    nbytes = spec_bytes(n_out.cpu().numpy(), c["K"], c["V"])
+    calls = 16
+    elapsed, per, clocks = _timed_graph(lambda: pa.spec_verify(p, q, draft, u, v), args.steps, args.warmup, dev,
+                                        calls)
+    peak, peak_kind = peaks()
+    call = float(np.mean(per))
+    hp, hq, hd, hu, hv = (t.cpu().pin_memory() for t in (p, q, draft, u, v))
+
+    def one():
+        for d_, h_ in ((p, hp), (q, hq), (draft, hd), (u, hu), (v, hv)):
+            d_.copy_(h_, non_blocking=True)
+        o, n = pa.spec_verify(p, q, draft, u, v)
+        o.cpu(), n.cpu()
+    one()
+    ne = max(3, args.steps // 5)
+    t0 = time.perf_counter()
+    for _ in range(ne):
+        one()
+    dt = (time.perf_counter() - t0) / ne
+    h2d = sum(t.numel() * t.element_size() for t in (hp, hq, hd, hu, hv))
+    line = {"metric": "speculative rejection sampling GB/s on 1 GB300 (fraction of HBM peak)",
+            "value": round(nbytes * args.steps * calls / (elapsed * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps * calls, "warmup": args.warmup * calls,
+            "ms_per_step": round(elapsed / (args.steps * calls), 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 probabilities, f32-pair sums",
+            "data": "synthetic (seeded)", "config": {"workload": "spec: " + DESCR[-2], **c,
+                                                     "accepted_drafts": int(n_out.sum().item() - c["B"]),
+                                                     "timing": f"{calls} calls per CUDA graph replay",
+                                                     "l2": "720 MB of distributions (no flush)"},
+            "sequences_per_s": round(c["B"] / (call * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (call * 1e-3) / 1e9, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                         "kernel": "pa_spec_verify call", "algorithmic_bytes_per_launch": nbytes,
+                         "avg_launch_ms": round(call, 5), "peak_kind": peak_kind},
+            "e2e": {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": int(out.numel() * 4 + n_out.numel() * 4), "ms_per_step": round(dt * 1e3, 3),
+                    "steps": ne},
+            "gpu_launches": args.steps * calls, "clocks": clocks}
+    if not args.no_cpu_baseline:
+        import oracle
+        nb = 16
+        args_h = [t[:nb].cpu().numpy() for t in (p, q, draft, u, v)]
+        t0 = time.perf_counter()
+        reps = 0
+        while reps == 0 or time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            ref, rn = oracle.spec_verify(*args_h)
+            reps += 1
+        dt = time.perf_counter() - t0
+        b2 = spec_bytes(rn, c["K"], c["V"])
+        line["cpu_baseline"] = {"value": round(reps * b2 / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{reps} passes over sequences 0..{nb - 1} ({b2} algorithmic bytes each) "
+                                          f"in {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------------------------- CPU oracle arm
 
 def oracle_sample(wl: synth.Workload, nseq: int):
@@ -587,6 +813,9 @@ def run_reference(args):
     if k == 0:
         run_prefill_reference(args)
         return
+    if k < 0:
+        run_aux_reference(args, k)
+        return
     wl = synth.workload(k, layers=1)
     nseq = pick_nseq(wl, args.ref_step_seconds)
     hk, hv, news, q = oracle_sample(wl, nseq)
@@ -633,6 +862,51 @@ def run_prefill_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_aux_reference(args, k: int):
+    """The oracle as the reference arm of the copy-on-write and rejection-sampling workloads."""
+    import oracle
+    if k == -1:
+        c = COW
+        shape = (c["num_blocks"], c["Hkv"], c["bs"], c["d"])
+        hk = np.zeros(shape, dtype=np.uint16)
+        hv = np.zeros(shape, dtype=np.uint16)
+        pairs = cow_pairs()
+        nbytes = 2 * len(pairs) * 2 * c["Hkv"] * c["bs"] * c["d"] * 2
+        step = lambda: oracle.copy_blocks(hk, hv, pairs)
+        metric, unit, sample = ("copy-on-write block copy GB/s on 1 GB300 (fraction of HBM peak)", "GB/s",
+                                "each step: the 4096 block pairs, K and V")
+    else:
+        c = SPEC
+        rng = np.random.default_rng(0x5EED0200)
+        nb = 8
+        p = rng.random((nb, c["K"] + 1, c["V"]), dtype=np.float32) ** 3
+        p /= p.sum(-1, keepdims=True)
+        q = rng.random((nb, c["K"], c["V"]), dtype=np.float32) ** 3
+        q /= q.sum(-1, keepdims=True)
+        draft = rng.integers(0, c["V"], size=(nb, c["K"]), dtype=np.int32)
+        u = rng.random((nb, c["K"]), dtype=np.float32)
+        v = rng.random(nb, dtype=np.float32)
+        _, rn = oracle.spec_verify(p, q, draft, u, v)
+        nbytes = spec_bytes(rn, c["K"], c["V"])
+        step = lambda: oracle.spec_verify(p, q, draft, u, v)
+        metric, unit, sample = ("speculative rejection sampling GB/s on 1 GB300 (fraction of HBM peak)", "GB/s",
+                                f"each step: {nb} sequences of the same shape")
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(nbytes / dt / 1e9, 4)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": dist_env()[0],
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 / raw words", "data": "synthetic (seeded)",
+            "config": {"workload": f"{args.workload}: {DESCR[k]}"},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -657,6 +931,10 @@ def main():
         run_reference(args)
     elif args.workload == "prefill":
         run_prefill(args)
+    elif args.workload == "cow":
+        run_cow(args)
+    elif args.workload == "spec":
+        run_spec(args)
     else:
         run_gpu(args)
 

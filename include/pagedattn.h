@@ -277,7 +277,8 @@ pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k
  * min(1, p/q)); the first rejected position is resampled from
  * max(0, p_i - q_i) renormalised (from p_i if that has no mass) and later
  * drafts are dropped; if all are kept, one more token is drawn from
- * p_num_draft. Draws use the inverse CDF at v_b, summed in fp64.
+ * p_num_draft. Draws use the inverse CDF at v_b, summed as float pairs
+ * (about 44 significant bits); a drawn token always has positive weight.
  *   p      device fp32 [num_seqs, num_draft + 1, vocab]  target distributions
  *   q      device fp32 [num_seqs, num_draft, vocab]      draft distributions
  *   draft  device int32 [num_seqs, num_draft]            a token outside the vocabulary counts as rejected

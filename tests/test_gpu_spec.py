@@ -1,8 +1,9 @@
 """Speculative rejection sampling on the GPU (pa_spec_verify) against the oracle.
 
 The accept decisions are fp32 comparisons taken the same way on both sides, so the number of kept
-drafts and the kept tokens must match exactly. The drawn token is an inverse CDF summed in fp64 in a
-different order on each side; it must match, or sit on a CDF boundary (checked with the oracle's sums)."""
+drafts and the kept tokens must match exactly. The drawn token is an inverse CDF, summed in fp64 by the
+oracle and in float pairs (about 44 significant bits, another order) by the kernel; it must match, or sit
+on a CDF boundary (checked with the oracle's fp64 sums)."""
 import numpy as np
 import pytest
 import torch
@@ -83,3 +84,63 @@ def test_lossless_in_distribution():
     freq = np.bincount(out[:, 0].cpu().numpy(), minlength=V) / B
     sigma = np.sqrt(p1 * (1 - p1) / B)
     assert (np.abs(freq - p1) < 5 * sigma + 1e-4).all(), (freq, p1)
+
+
+def test_residual_without_mass_draws_from_target():
+    """p == q with zeros; every draft sits on a zero-probability token, so it is rejected at position 0 and
+    max(0, p - q) has no mass: the token is drawn from p itself."""
+    rng = np.random.default_rng(11)
+    B, K, V = 48, 3, 4099
+    p = _dist(rng, (B, K + 1, V))
+    p[:, :, ::3] = 0
+    p /= p.sum(-1, keepdims=True)
+    q = p[:, :K].copy()
+    draft = np.zeros((B, K), np.int32)                      # token 0 has zero probability
+    u = rng.random((B, K)).astype(np.float32)
+    v = rng.random(B).astype(np.float32)
+    out, n = _check(p, q, draft, u, v)
+    assert (n == 1).all()
+    assert (p[np.arange(B), 0, out[:, 0]] > 0).all()
+
+
+@pytest.mark.parametrize("vv", [0.0, np.nextafter(np.float32(1), np.float32(0))])
+def test_extreme_uniforms(vv):
+    """v = 0 draws the first token of positive weight; v just below 1 puts the target next to the total,
+    where the kernel's sums may round past it: the token must still match (or sit on a boundary) and
+    carry positive weight."""
+    B, K, V = 32, 2, 128256
+    p, q, draft, u, _ = _case(99, B, K, V, agree=0.5)
+    v = np.full(B, vv, np.float32)
+    out, n = _check(p, q, draft, u, v)
+    for b in range(B):
+        k = n[b] - 1
+        row = k if k < K else K
+        w = np.maximum(p[b, row].astype(np.float64) - (q[b, row].astype(np.float64) if k < K else 0), 0)
+        if not w.any():
+            w = np.maximum(p[b, row].astype(np.float64), 0)
+        assert w[out[b, k]] > 0
+        if vv == 0.0:
+            assert out[b, k] == np.flatnonzero(w > 0)[0]
+
+
+@pytest.mark.parametrize("V", [50257, 129, 1 << 17])
+def test_sparse_rows(V):
+    """Mass on a few scattered tokens (most segments of the row are empty), odd and power-of-two sizes."""
+    rng = np.random.default_rng(V)
+    B, K = 24, 4
+    p = np.zeros((B, K + 1, V), np.float32)
+    q = np.zeros((B, K, V), np.float32)
+    for b in range(B):
+        for i in range(K + 1):
+            idx = rng.choice(V, size=min(V, 7), replace=False)
+            p[b, i, idx] = rng.random(len(idx)) + 0.01
+        for i in range(K):
+            idx = rng.choice(V, size=min(V, 7), replace=False)
+            q[b, i, idx] = rng.random(len(idx)) + 0.01
+    p /= p.sum(-1, keepdims=True)
+    q /= q.sum(-1, keepdims=True)
+    draft = np.stack([[rng.choice(V, p=q[b, i].astype(np.float64) / q[b, i].astype(np.float64).sum()) for i in range(K)]
+                      for b in range(B)]).astype(np.int32)
+    u = rng.random((B, K)).astype(np.float32)
+    v = rng.random(B).astype(np.float32)
+    _check(p, q, draft, u, v)
