@@ -10,7 +10,8 @@
 //      segments with coalesced float4 loads (eight chunks in flight per lane) into shared memory;
 //   2. warp 0 scans the 256 segment sums and finds the first segment whose running sum passes
 //      v * total;
-//   3. warp 0 walks that segment a chunk at a time (lane sums, an ordered warp scan) to the token.
+//   3. warp 0 walks that segment 512 values at a time (16 per lane: lane sums, an ordered warp scan,
+//      then the one lane where the running sum passes the target walks its values) to the token.
 // Sums are double-single (a float pair hi + lo: Knuth's two-sum, Dekker's fast two-sum, and the
 // compensated sum of Ogita, Rump and Oishi within a lane), about 44 significant bits: near the fp64
 // sums of the definition at the fp32 rate, as fp64 arithmetic is scarce on this part. A weight
@@ -25,7 +26,6 @@ constexpr int SPEC_SEGS = 256;                         // segments per row
 constexpr int SPEC_SEGS_WARP = SPEC_SEGS / SPEC_WARPS; // 16 consecutive segments summed by one warp
 constexpr int SPEC_SEGS_LANE = SPEC_SEGS / 32;         // 8 consecutive segments per lane when locating
 constexpr int SPEC_SUM_UNROLL = 8;                     // chunks a lane has in flight while summing
-constexpr int SPEC_UNROLL = 4;                         // chunks a lane has in flight in the walk
 constexpr int SPEC_CH = 512;                           // values per bulk copy chunk
 constexpr int SPEC_NS = 3;                             // chunks in flight per warp (bulk variant)
 constexpr uint32_t SPEC_STAGE_BYTES = 2 * SPEC_CH * 4; // p then q
@@ -52,7 +52,16 @@ __device__ __forceinline__ DSum ds_add(DSum a, DSum b) {
     return DSum{hi, __fsub_rn(e, __fsub_rn(hi, s))};
 }
 
-__device__ __forceinline__ double ds_value(DSum a) { return (double)a.hi + (double)a.lo; }
+// a > b for normalised pairs (|lo| at most half an ulp of hi, as ds_add leaves them).
+__device__ __forceinline__ bool ds_gt(DSum a, DSum b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
+// v * t as a normalised pair: the fma gives the exact error of v * t.hi.
+__device__ __forceinline__ DSum ds_scale(float v, DSum t) {
+    const float p = __fmul_rn(v, t.hi);
+    const float lo = __fmaf_rn(v, t.lo, __fmaf_rn(v, t.hi, -p));
+    const float hi = __fadd_rn(p, lo);
+    return DSum{hi, __fsub_rn(lo, __fsub_rn(hi, p))};
+}
 
 // Weight of one vocabulary entry: max(0, p - q) (residual) or max(0, p), exactly as a pair. For the
 // residual, d = p - q rounded and e = (p - d) - q is Dekker's fast two-sum, exact whenever p >= q >= 0,
@@ -255,14 +264,14 @@ __device__ __forceinline__ void segment_sums_direct(const SpecRow &row, int64_t 
 }
 
 template <bool kBulk>
-__global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *p, const float *q,
+__global__ void __launch_bounds__(SPEC_THREADS, 1) spec_verify_kernel(const float *p, const float *q,
                                                                     const int32_t *draft, const float *u,
                                                                     const float *v, int K, int64_t V, int32_t *out,
                                                                     int32_t *n_out, int *status) {
     extern __shared__ __align__(128) uint8_t spec_smem[];
     __shared__ DSum s_seg[SPEC_SEGS];
     __shared__ DSum s_before;
-    __shared__ double s_target;
+    __shared__ DSum s_target;
     __shared__ int s_rej, s_sel, s_abort;
     const int64_t b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -274,6 +283,7 @@ __global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *
     }
     if (tid == 0) s_abort = 0;
 
+    const float vb = warp == 0 ? v[b] : 0.f;            // in flight during the accept tests
     if (warp == 0) {
         // accept tests, 32 drafts at a time; the first failure (or out-of-vocabulary draft) ends them
         int rej = K;
@@ -313,7 +323,6 @@ __global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *
     // segments: whole copy chunks (bulk) or whole 128-value chunks, 256 of them covering the row
     constexpr int64_t unit = kBulk ? SPEC_CH : 128;
     const int64_t seg_len = ((V + SPEC_SEGS - 1) / SPEC_SEGS + unit - 1) / unit * unit;
-    const int nch = (int)(seg_len / 128);
     uint32_t issued = 0;
 
     for (int pass = 0; pass < 2; ++pass) {
@@ -340,23 +349,22 @@ __global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *
         }
         // level 2: the first segment whose running sum passes v * total
         if (warp == 0) {
-            DSum sv[SPEC_SEGS_LANE], mine{0.f, 0.f};
+            static_assert(SPEC_SEGS_LANE == 8, "level 2 sums a lane's segments as a tree of 8");
+            DSum sv[SPEC_SEGS_LANE];
 #pragma unroll
-            for (int j = 0; j < SPEC_SEGS_LANE; ++j) {
-                sv[j] = s_seg[lane * SPEC_SEGS_LANE + j];
-                mine = ds_add(mine, sv[j]);
-            }
+            for (int j = 0; j < SPEC_SEGS_LANE; ++j) sv[j] = s_seg[lane * SPEC_SEGS_LANE + j];
+            const DSum mine = ds_add(ds_add(ds_add(sv[0], sv[1]), ds_add(sv[2], sv[3])),
+                                     ds_add(ds_add(sv[4], sv[5]), ds_add(sv[6], sv[7])));
             DSum incl, excl;
             warp_scan(mine, lane, incl, excl);
-            const double total = ds_value(shfl_ds(incl, 31));
-            const double target = (double)v[b] * total;
+            const DSum target = ds_scale(vb, shfl_ds(incl, 31));
             DSum c = excl, before{0.f, 0.f};
             int first = -1, last = -1;
 #pragma unroll
             for (int j = 0; j < SPEC_SEGS_LANE; ++j) {
                 const DSum nc = ds_add(c, sv[j]);
                 if (sv[j].hi > 0.f) {
-                    if (first < 0 && ds_value(nc) > target) {
+                    if (first < 0 && ds_gt(nc, target)) {
                         first = j;
                         before = c;
                     }
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *
                 if (lane == ll) {
                     s_sel = lane * SPEC_SEGS_LANE + last;
                     s_before = DSum{0.f, 0.f};
-                    s_target = __longlong_as_double(0x7ff0000000000000ll);  // +inf: nothing passes it
+                    s_target = DSum{__int_as_float(0x7f800000), 0.f};  // +inf: nothing passes it
                 }
             } else if (lane == 0) {
                 s_sel = -1;                            // no mass at all
@@ -392,42 +400,64 @@ __global__ void __launch_bounds__(SPEC_THREADS) spec_verify_kernel(const float *
         __syncthreads();
     }
 
-    // level 3: walk the chosen segment, a chunk of 128 values at a time
+    // level 3: walk the chosen segment in blocks of 512 values, 16 consecutive values per lane: lane sums,
+    // one ordered warp scan, and the lane where the running sum passes the target walks its 16 values
     if (warp == 0) {
         const int sel = s_sel;
         int tok = -1;
         if (sel >= 0) {
-            const double target = s_target;
+            const DSum target = s_target;
             const int64_t s0 = sel * seg_len;
             const int64_t s1 = s0 + seg_len < V ? s0 + seg_len : V;
             DSum run = s_before;
             int64_t last = -1;
-            for (int k = 0; k < nch && tok < 0; k += SPEC_UNROLL) {
-                float4 a[SPEC_UNROLL], c[SPEC_UNROLL];
+            for (int64_t blk = s0; blk < s1 && tok < 0; blk += 512) {
+                const int64_t i0 = blk + lane * 16;
+                DSum w[16];
 #pragma unroll
-                for (int j = 0; j < SPEC_UNROLL; ++j)
-                    load4(row, s0 + (int64_t)(k + j) * 128 + lane * 4, k + j < nch ? s1 : 0, a[j], c[j]);
+                for (int j = 0; j < 4; ++j) {
+                    float4 a, c;
+                    load4(row, i0 + 4 * j, s1, a, c);
+                    DSum w4[4];
+                    weights4(a, c, row.residual, w4);
 #pragma unroll
-                for (int j = 0; j < SPEC_UNROLL; ++j) {
-                    if (tok >= 0) break;                   // warp-uniform
-                    const int64_t i = s0 + (int64_t)(k + j) * 128 + lane * 4;
-                    DSum w[4];
-                    weights4(a[j], c[j], row.residual, w);
-                    const DSum mine = ds_add(ds_add(w[0], w[1]), ds_add(w[2], w[3]));
-                    DSum incl, excl;
-                    warp_scan(mine, lane, incl, excl);
-                    DSum cs = ds_add(run, excl);
-                    int t = -1;
+                    for (int e = 0; e < 4; ++e) w[4 * j + e] = w4[e];
+                }
+                DSum t8[8], t4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        cs = ds_add(cs, w[e]);
-                        if (w[e].hi > 0.f) {
-                            if (t < 0 && ds_value(cs) > target) t = (int)(i + e);
-                            last = i + e;
-                        }
+                for (int k = 0; k < 8; ++k) t8[k] = ds_add(w[2 * k], w[2 * k + 1]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) t4[k] = ds_add(t8[2 * k], t8[2 * k + 1]);
+                const DSum mine = ds_add(ds_add(t4[0], t4[1]), ds_add(t4[2], t4[3]));
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (w[e].hi > 0.f) last = i0 + e;
+                DSum incl, excl;
+                warp_scan(mine, lane, incl, excl);
+                const unsigned hit = __ballot_sync(0xffffffffu, mine.hi > 0.f && ds_gt(ds_add(run, incl), target));
+                if (hit) {
+                    // spread lane fl's 16 values over lanes 0..15 and scan them from its running sum
+                    const int fl = __ffs(hit) - 1;
+                    DSum we{0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const DSum x = shfl_ds(w[e], fl);
+                        if (lane == e) we = x;
                     }
-                    const unsigned hit = __ballot_sync(0xffffffffu, t >= 0);
-                    if (hit) tok = __shfl_sync(0xffffffffu, t, __ffs(hit) - 1);
+                    DSum ie = we;
+#pragma unroll
+                    for (int d = 1; d < 16; d <<= 1) {
+                        const DSum up = shfl_up_ds(ie, d);
+                        if (lane >= d) ie = ds_add(up, ie);
+                    }
+                    const DSum base = shfl_ds(ds_add(run, excl), fl);
+                    const bool pos = lane < 16 && we.hi > 0.f;
+                    const unsigned pass = __ballot_sync(0xffffffffu, pos && ds_gt(ds_add(base, ie), target));
+                    const unsigned posm = __ballot_sync(0xffffffffu, pos);
+                    // the first value passing the target, else (rounding) the lane's last positive value
+                    const int e = pass ? __ffs(pass) - 1 : 31 - __clz(posm);
+                    tok = (int)(__shfl_sync(0xffffffffu, i0, fl) + e);
+                } else {
                     run = ds_add(run, shfl_ds(incl, 31));
                 }
             }
