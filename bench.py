@@ -70,22 +70,30 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def decode_source_sha() -> str:
+TRAFFIC_SOURCES = {
+    "decode": ("decode.cu", "pa_device.cuh", "pa_internal.h"),
+    "spec": ("spec_verify.cu", "pa_device.cuh", "pa_internal.h"),
+    "cow": ("copy_blocks.cu", "pa_device.cuh", "pa_internal.h"),
+    "prefill": ("prefill.cu", "pa_device.cuh", "pa_internal.h"),
+}
+
+
+def source_sha(kernel: str = "decode") -> str:
     h = hashlib.sha256()
-    for fn in ("decode.cu", "pa_device.cuh", "pa_internal.h"):
+    for fn in TRAFFIC_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_cache_223_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def measured_traffic(workload: str, kernel: str = "decode"):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "kernel_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_sha") == decode_source_sha():
+        if e and e.get("source_sha") == source_sha(kernel):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -508,7 +516,7 @@ def run_prefill(args):
                        "l2": "8 layer pools (1.2 GB of K/V) cycle through L2 (no flush)",
                        "parallelism": f"replicas{ws}"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4), "traffic": measured_traffic("prefill", "prefill"),
                          "kernel": "pa_prefill call (prefill kernel)", "algorithmic_flops_per_launch": flops_call,
                          "avg_launch_ms": round(call_avg, 5), "peak_kind": peak_kind},
             "e2e": e2e,
@@ -594,21 +602,25 @@ def run_cow(args):
     elapsed, per, clocks = _timed(lambda: pa.copy_blocks(pool, pairs), args.steps, args.warmup, dev)
     assert pool.check() == 0
     # end to end: pairs from pinned host memory, the copy, one destination block read back
-    host_pairs = torch.from_numpy(pairs_h).pin_memory()
-    back = torch.empty((c["Hkv"], c["bs"], c["d"]), dtype=torch.float16).pin_memory()
-    dst0 = int(pairs_h[0, 1])
+    e2e = None
+    if not args.no_e2e:
+        host_pairs = torch.from_numpy(pairs_h).pin_memory()
+        back = torch.empty((c["Hkv"], c["bs"], c["d"]), dtype=torch.float16).pin_memory()
+        dst0 = int(pairs_h[0, 1])
 
-    def one():
-        pairs.copy_(host_pairs, non_blocking=True)
-        pa.copy_blocks(pool, pairs)
-        back.copy_(pool.k_cache[dst0], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-    one()
-    n = max(3, args.steps // 5)
-    t0 = time.perf_counter()
-    for _ in range(n):
+        def one():
+            pairs.copy_(host_pairs, non_blocking=True)
+            pa.copy_blocks(pool, pairs)
+            back.copy_(pool.k_cache[dst0], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
         one()
-    dt = (time.perf_counter() - t0) / n
+        n = max(3, args.steps // 5)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            one()
+        dt = (time.perf_counter() - t0) / n
+        e2e = {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(pairs_h.nbytes),
+               "d2h_bytes_per_step": block_bytes, "ms_per_step": round(dt * 1e3, 3), "steps": n}
     peak, peak_kind = peaks()
     call = float(np.mean(per))
     line = {"metric": "copy-on-write block copy GB/s on 1 GB300 (fraction of HBM peak)",
@@ -618,12 +630,13 @@ def run_cow(args):
             "data": "synthetic", "config": {"workload": "cow: " + DESCR[-1], **c,
                                             "l2": "2 x 512 MB moved per step (no flush)"},
             "roofline": {"bound": "hbm", "achieved": round(nbytes / (call * 1e-3) / 1e9, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4),
+                         "traffic": measured_traffic("cow", "cow"),
                          "kernel": "pa_copy_blocks call", "algorithmic_bytes_per_launch": nbytes,
                          "avg_launch_ms": round(call, 5), "peak_kind": peak_kind},
-            "e2e": {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(pairs_h.nbytes),
-                    "d2h_bytes_per_step": block_bytes, "ms_per_step": round(dt * 1e3, 3), "steps": n},
             "gpu_launches": args.steps, "clocks": clocks}
+    if e2e:
+        line["e2e"] = e2e
     if not args.no_cpu_baseline:
         import oracle
         shape = (c["num_blocks"], c["Hkv"], c["bs"], c["d"])
@@ -691,20 +704,25 @@ def run_spec(args):
                                         calls)
     peak, peak_kind = peaks()
     call = float(np.mean(per))
-    hp, hq, hd, hu, hv = (t.cpu().pin_memory() for t in (p, q, draft, u, v))
+    e2e = None
+    if not args.no_e2e:
+        hp, hq, hd, hu, hv = (t.cpu().pin_memory() for t in (p, q, draft, u, v))
 
-    def one():
-        for d_, h_ in ((p, hp), (q, hq), (draft, hd), (u, hu), (v, hv)):
-            d_.copy_(h_, non_blocking=True)
-        o, n = pa.spec_verify(p, q, draft, u, v)
-        o.cpu(), n.cpu()
-    one()
-    ne = max(3, args.steps // 5)
-    t0 = time.perf_counter()
-    for _ in range(ne):
+        def one():
+            for d_, h_ in ((p, hp), (q, hq), (draft, hd), (u, hu), (v, hv)):
+                d_.copy_(h_, non_blocking=True)
+            o, n = pa.spec_verify(p, q, draft, u, v)
+            o.cpu(), n.cpu()
         one()
-    dt = (time.perf_counter() - t0) / ne
-    h2d = sum(t.numel() * t.element_size() for t in (hp, hq, hd, hu, hv))
+        ne = max(3, args.steps // 5)
+        t0 = time.perf_counter()
+        for _ in range(ne):
+            one()
+        dt = (time.perf_counter() - t0) / ne
+        h2d = sum(t.numel() * t.element_size() for t in (hp, hq, hd, hu, hv))
+        e2e = {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": int(out.numel() * 4 + n_out.numel() * 4), "ms_per_step": round(dt * 1e3, 3),
+               "steps": ne}
     line = {"metric": "speculative rejection sampling GB/s on 1 GB300 (fraction of HBM peak)",
             "value": round(nbytes * args.steps * calls / (elapsed * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps * calls, "warmup": args.warmup * calls,
@@ -716,13 +734,13 @@ def run_spec(args):
                                                      "l2": "720 MB of distributions (no flush)"},
             "sequences_per_s": round(c["B"] / (call * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(nbytes / (call * 1e-3) / 1e9, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(nbytes / (call * 1e-3) / 1e9 / peak, 4),
+                         "traffic": measured_traffic("spec", "spec"),
                          "kernel": "pa_spec_verify call", "algorithmic_bytes_per_launch": nbytes,
                          "avg_launch_ms": round(call, 5), "peak_kind": peak_kind},
-            "e2e": {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": int(out.numel() * 4 + n_out.numel() * 4), "ms_per_step": round(dt * 1e3, 3),
-                    "steps": ne},
             "gpu_launches": args.steps * calls, "clocks": clocks}
+    if e2e:
+        line["e2e"] = e2e
     if not args.no_cpu_baseline:
         import oracle
         nb = 16
