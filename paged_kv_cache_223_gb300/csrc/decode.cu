@@ -594,6 +594,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
 #pragma unroll 8
         for (int pp = grp; pp < nparts; pp += groups) {
             const float c = w[pp];
+            if (c == 0.f) continue;                    // an empty partition: its O is not read (it may be unwritten)
             const float4 x = __ldcg(po + (int64_t)pp * (D / 4));
             acc.x += c * x.x;
             acc.y += c * x.y;

@@ -60,6 +60,10 @@ constexpr int PF_NBAR = 2 * PF_KSTAGES + 2 * PF_VSTAGES + 3 * PF_QT + 1;
 constexpr int PF_SMEM = 1024 + PF_OFF_BAR + PF_NBAR * 8 + 16;
 constexpr uint32_t PF_TMEM_COLS = 512;                        // row tile t: S/P at 256 t, O at 256 t + 128
 constexpr float PF_RESCALE_LOG2 = 8.f;                        // stale-max headroom (P <= 2^8)
+// epilogue staging of a warp's 32 output rows (fp32) in the copy rings; the padded row stride keeps
+// both the per-thread row writes and the per-row warp reads free of bank conflicts
+constexpr int PF_STAGE_STRIDE = PF_D + 4;
+static_assert(8 * 32 * PF_STAGE_STRIDE * 4 <= PF_KSTAGES * PF_KV_BYTES + PF_VSTAGES * PF_KV_BYTES, "epilogue staging");
 static_assert(PF_SUB * 2 <= 32, "one copy per producer lane");
 static_assert(PF_SMEM <= 227 * 1024, "prefill shared memory");
 
@@ -317,12 +321,27 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     } else {
         setmaxnreg_inc<PF_REGS_SOFTMAX>();
         {
-            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + orow * PF_D);
-            uint8_t *qdst = smem + t_of * PF_Q_BYTES + rt * 128;
+            // the warp's 32 Q rows, two per load (16 lanes x 16 bytes = one 256-byte row, coalesced), into
+            // 16 chunks of 8 values per row with the 128-byte swizzle
+            uint8_t *qtile = smem + t_of * PF_Q_BYTES;
+            const int c = lane & 15;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {                     // 16 chunks of 8 values, 128-byte swizzle
-                const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(qdst + (c >> 3) * (PF_BM * 128) + (((c & 7) ^ (rt & 7)) << 4)) = v;
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int src = 2 * (k0 + k) + (lane >> 4);
+                    const int64_t orow_k = __shfl_sync(0xffffffffu, orow, src);
+                    const bool ok_k = __shfl_sync(0xffffffffu, row_ok, src);
+                    v[k] = ok_k ? __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + orow_k * PF_D) + c)
+                                : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rt_k = (warp & 3) * 32 + 2 * (k0 + k) + (lane >> 4);
+                    *reinterpret_cast<uint4 *>(qtile + rt_k * 128 + (c >> 3) * (PF_BM * 128) +
+                                               (((c & 7) ^ (rt_k & 7)) << 4)) = v[k];
+                }
             }
             fence_proxy_async_smem();
             named_barrier_sync(Q_BARRIER, Q_BARRIER_THREADS);
@@ -413,49 +432,44 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_o_done + t * 8, 0u, p.wait_ns));
         if (!ok) {
             if (lane == 0) *abort_flag = 1;
-        } else if (nt > 0 && CASCADE) {
-            // unnormalised state of the chunk's keys in its first partition slot; the chunk's other
-            // slots are written empty (sum 0, zero O) so that the merge gives them no weight
-            tc_fence_after();
-            const int slot0 = key0 / p.part_tokens, slot1 = L / p.part_tokens;
-            const int64_t prow = orow * p.max_parts + slot0;
-            float *dst = p.part_o + prow * PF_D;
-#pragma unroll
-            for (int c0 = 0; c0 < PF_D; c0 += 32) {
-                float a[32];
-                tmem_ld32(tmem_o + c0, a);
-                if (row_ok) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
-                }
-            }
-            if (row_ok) {
-                p.part_ml[prow] = make_float2(m_ref, l);
-                for (int sl = slot0 + 1; sl < slot1; ++sl) {
-                    float4 *z = reinterpret_cast<float4 *>(p.part_o + (orow * p.max_parts + sl) * PF_D);
-#pragma unroll 4
-                    for (int c = 0; c < PF_D / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    p.part_ml[orow * p.max_parts + sl] = make_float2(0.f, 0.f);
-                }
-            }
         } else if (nt > 0) {
+            // the warp's 32 output rows go through the free copy rings (all MMAs have completed and every
+            // copy was consumed): each thread stages its row, then the warp stores row by row, coalesced.
+            // A cascade writes the unnormalised state of the chunk's keys in its first partition slot; the
+            // chunk's other slots get sum 0, which the merge reads as empty
             tc_fence_after();
-            const float inv = 1.f / l;
-            T *dst = reinterpret_cast<T *>(p.out) + orow * PF_D;
+            float *stage = reinterpret_cast<float *>(smem + PF_OFF_K) + warp * 32 * PF_STAGE_STRIDE;
+            float *mine = stage + lane * PF_STAGE_STRIDE;
+            const float sc = CASCADE ? 1.f : 1.f / l;
 #pragma unroll
             for (int c0 = 0; c0 < PF_D; c0 += 32) {
                 float a[32];
                 tmem_ld32(tmem_o + c0, a);
-                if (row_ok) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        const uint4 v =
-                            make_uint4(pack2<T>(a[c] * inv, a[c + 1] * inv), pack2<T>(a[c + 2] * inv, a[c + 3] * inv),
-                                       pack2<T>(a[c + 4] * inv, a[c + 5] * inv), pack2<T>(a[c + 6] * inv, a[c + 7] * inv));
-                        *reinterpret_cast<uint4 *>(dst + c0 + c) = v;
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(mine + c0 + c) = make_float4(a[c] * sc, a[c + 1] * sc, a[c + 2] * sc,
+                                                                             a[c + 3] * sc);
+            }
+            __syncwarp();
+            const int slot0 = CASCADE ? key0 / p.part_tokens : 0;
+#pragma unroll 4
+            for (int k = 0; k < 32; ++k) {
+                const int64_t orow_k = __shfl_sync(0xffffffffu, orow, k);
+                const bool ok_k = __shfl_sync(0xffffffffu, row_ok, k);
+                const float4 x = *reinterpret_cast<const float4 *>(stage + k * PF_STAGE_STRIDE + lane * 4);
+                if (ok_k) {
+                    if constexpr (CASCADE) {
+                        *reinterpret_cast<float4 *>(p.part_o + (orow_k * p.max_parts + slot0) * PF_D + lane * 4) = x;
+                    } else {
+                        T *dst = reinterpret_cast<T *>(p.out) + orow_k * PF_D + lane * 4;
+                        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack2<T>(x.x, x.y), pack2<T>(x.z, x.w));
                     }
                 }
+            }
+            if (CASCADE && row_ok) {
+                const int slot1 = L / p.part_tokens;
+                p.part_ml[orow * p.max_parts + slot0] = make_float2(m_ref, l);
+                for (int sl = slot0 + 1; sl < slot1; ++sl) p.part_ml[orow * p.max_parts + sl] = make_float2(0.f, 0.f);
             }
         }
     }
