@@ -623,6 +623,60 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
     }
 }
 
+// The same merge with one warp per output row, for at most 32 partitions: lane pp holds partition
+// pp's (max, sum), the weights and their sum come from warp shuffles, and each lane accumulates
+// D / 32 dims over the partitions in order. No block barrier; two dependent rounds of loads.
+constexpr int MERGE_ROW_WARPS = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const DecodeParams p) {
+    static_assert(D % 32 == 0 && D / 32 <= 4, "dims per lane");
+    constexpr int DL = D / 32;                     // dims per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * MERGE_ROW_WARPS + warp;   // (b * q_len + qi) * Hq + h
+    if (row >= (int64_t)p.num_seqs * p.q_len * p.Hq) return;
+    const int b = (int)(row / p.Hq) / p.q_len;
+    int L = __ldg(p.context_lens + b);
+    L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
+    const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
+    if (nparts <= 1) return;
+    const float2 v = lane < nparts ? __ldcg(p.part_ml + row * p.max_parts + lane) : make_float2(0.f, 0.f);
+    float M = v.y > 0.f ? v.x : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+    float ds = w * v.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
+    const float *po = p.part_o + row * p.max_parts * D + lane * DL;
+    float acc[DL];
+#pragma unroll
+    for (int i = 0; i < DL; ++i) acc[i] = 0.f;
+#pragma unroll 4
+    for (int pp = 0; pp < nparts; ++pp) {
+        const float c = __shfl_sync(0xffffffffu, w, pp);
+        if (c == 0.f) continue;                    // an empty partition: its O is not read (it may be unwritten)
+        if constexpr (DL == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)pp * D));
+            acc[0] += c * x.x;
+            acc[1] += c * x.y;
+            acc[2] += c * x.z;
+            acc[3] += c * x.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < DL; ++i) acc[i] += c * __ldcg(po + (int64_t)pp * D + i);
+        }
+    }
+    const float inv = 1.f / ds;
+    T *out = reinterpret_cast<T *>(p.out) + row * D + lane * DL;
+    if constexpr (DL == 4) {
+        *reinterpret_cast<uint2 *>(out) = make_uint2(pack2<T>(acc[0] * inv, acc[1] * inv), pack2<T>(acc[2] * inv, acc[3] * inv));
+    } else {
+#pragma unroll
+        for (int i = 0; i < DL; i += 2) *reinterpret_cast<uint32_t *>(out + i) = pack2<T>(acc[i] * inv, acc[i + 1] * inv);
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 
 template <typename T, int D, int NT, bool KV8>
@@ -683,6 +737,18 @@ int merge_splits_for(int64_t units, int G, int head_dim, int sm_count) {
 }
 
 cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
+    if (p.max_parts <= 32) {
+        const int64_t rows = (int64_t)p.num_seqs * p.q_len * p.Hq;
+        const unsigned grid = (unsigned)((rows + MERGE_ROW_WARPS - 1) / MERGE_ROW_WARPS);
+        if (dtype == PA_FP16) {
+            if (head_dim == 128) merge_rows_kernel<__half, 128><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+            else merge_rows_kernel<__half, 64><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+        } else {
+            if (head_dim == 128) merge_rows_kernel<__nv_bfloat16, 128><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+            else merge_rows_kernel<__nv_bfloat16, 64><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+        }
+        return cudaGetLastError();
+    }
     const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv * p.merge_splits;
     const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim, p.merge_splits);
     const int pps = (p.G * (head_dim / 4) + p.merge_splits - 1) / p.merge_splits;
