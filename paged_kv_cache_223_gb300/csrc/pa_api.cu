@@ -380,14 +380,15 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
             }
         }
     }
-    // the prefix kernel (tensor cores, one CTA per SM) runs on the pool's side stream beside the suffix
-    // decode (bandwidth, many small CTAs) on the caller's stream; the merge waits for both
+    // the prefix kernel (tensor cores, one CTA per SM) goes first, straight onto the caller's stream, so
+    // that its CTAs take whole SMs before the suffix decode (bandwidth, many small CTAs, on the pool's
+    // side stream) fills the rest; the merge waits for both
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     std::lock_guard<std::mutex> lk(pool->mu);
     if (cudaEventRecord(pool->ev_fork, s) != cudaSuccess || cudaStreamWaitEvent(pool->side, pool->ev_fork, 0) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (launch_prefix(p, c.dtype, tmk, tmv, pool->side) != cudaSuccess) return PA_ERR_CUDA;
-    if (launch_decode(p, c.dtype, c.head_dim, tmk, tmv, s, false) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_prefix(p, c.dtype, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_decode(p, c.dtype, c.head_dim, tmk, tmv, pool->side, false) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaEventRecord(pool->ev_join, pool->side) != cudaSuccess || cudaStreamWaitEvent(s, pool->ev_join, 0) != cudaSuccess)
         return PA_ERR_CUDA;
     p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, c.head_dim, pool->sm_count);
