@@ -894,21 +894,16 @@ def run_aux_reference(args, k: int):
         metric, unit, sample = ("copy-on-write block copy GB/s on 1 GB300 (fraction of HBM peak)", "GB/s",
                                 "each step: the 4096 block pairs, K and V")
     else:
+        import torch
         c = SPEC
-        rng = np.random.default_rng(0x5EED0200)
         nb = 8
-        p = rng.random((nb, c["K"] + 1, c["V"]), dtype=np.float32) ** 3
-        p /= p.sum(-1, keepdims=True)
-        q = rng.random((nb, c["K"], c["V"]), dtype=np.float32) ** 3
-        q /= q.sum(-1, keepdims=True)
-        draft = rng.integers(0, c["V"], size=(nb, c["K"]), dtype=np.int32)
-        u = rng.random((nb, c["K"]), dtype=np.float32)
-        v = rng.random(nb, dtype=np.float32)
+        # the GPU arm's recipe on the host generator; the first nb sequences
+        p, q, draft, u, v = (t[:nb].numpy().copy() for t in spec_inputs(torch.device("cpu")))
         _, rn = oracle.spec_verify(p, q, draft, u, v)
         nbytes = spec_bytes(rn, c["K"], c["V"])
         step = lambda: oracle.spec_verify(p, q, draft, u, v)
         metric, unit, sample = ("speculative rejection sampling GB/s on 1 GB300 (fraction of HBM peak)", "GB/s",
-                                f"each step: {nb} sequences of the same shape")
+                                f"each step: the first {nb} of the {c['B']} sequences (same recipe, host generator)")
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -919,7 +914,7 @@ def run_aux_reference(args, k: int):
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": dist_env()[0],
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 / raw words", "data": "synthetic (seeded)",
-            "config": {"workload": f"{args.workload}: {DESCR[k]}"},
+            "config": {"workload": f"{args.workload}: {DESCR[k]}", **c},
             "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
