@@ -55,7 +55,7 @@ __host__ __device__ constexpr int ring_bytes(int D, bool kv8) {
            (kv8 ? ((scale_region(kv8) + 1023) & ~1023) : 0);
 }
 __host__ __device__ constexpr int merge_bytes(int D, int nt) {
-    return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4;
+    return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4 + nt * 8 * (DECODE_WARPS + 2) * 4;
 }
 __host__ __device__ constexpr int body_bytes(int D, int nt, bool kv8) {
     return ring_bytes(D, kv8) > merge_bytes(D, nt) ? ring_bytes(D, kv8) : merge_bytes(D, nt);
@@ -101,6 +101,38 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     const int g = bg % p.Hkv;
     const int b = bg / p.Hkv;
 
+    // ---- query fragments: B operand (col-major 16 x 8) of S^T = K . Q^T (loaded first: their latency
+    // overlaps the context length and block table loads below)
+    const int gq = lane >> 2;   // MMA group id: key row within an 8-row half; query column for B
+    const int tq = lane & 3;    // thread in group
+    uint32_t qf[NT][KSTEPS][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int r = nt * 8 + gq;
+        if (r < p.rows) {
+            const int qi = r / p.G, hh = r - (r / p.G) * p.G;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                reinterpret_cast<const T *>(p.q) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * D);
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                // FP8 pools: the K codes reach the MMA with each lane holding 4 consecutive dims
+                // (16 ks + 4 tq ..), so the contraction index is permuted the same way for Q
+                qf[nt][ks][0] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq : tq));
+                qf[nt][ks][1] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq + 1 : 4 + tq));
+                if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const __nv_bfloat162 bq = *reinterpret_cast<const __nv_bfloat162 *>(&qf[nt][ks][e]);
+                        const float2 f = __bfloat1622float2(bq);
+                        qf[nt][ks][e] = pack2<__half>(f.x, f.y);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
+        }
+    }
     // ---- context of this sequence, clamped to what the table / launch can hold
     int L = __ldg(p.context_lens + b);
     if (L < p.q_len || L > p.max_ctx) {
@@ -179,37 +211,6 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     }
     issued = my_tiles < STAGES ? my_tiles : STAGES;
 
-    // ---- query fragments: B operand (col-major 16 x 8) of S^T = K . Q^T
-    const int gq = lane >> 2;   // MMA group id: key row within an 8-row half; query column for B
-    const int tq = lane & 3;    // thread in group
-    uint32_t qf[NT][KSTEPS][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int r = nt * 8 + gq;
-        if (r < p.rows) {
-            const int qi = r / p.G, hh = r - (r / p.G) * p.G;
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                reinterpret_cast<const T *>(p.q) + (((int64_t)b * p.q_len + qi) * p.Hq + g * p.G + hh) * D);
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                // FP8 pools: the K codes reach the MMA with each lane holding 4 consecutive dims
-                // (16 ks + 4 tq ..), so the contraction index is permuted the same way for Q
-                qf[nt][ks][0] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq : tq));
-                qf[nt][ks][1] = __ldg(qrow + ks * 8 + (KV8 ? 2 * tq + 1 : 4 + tq));
-                if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const __nv_bfloat162 bq = *reinterpret_cast<const __nv_bfloat162 *>(&qf[nt][ks][e]);
-                        const float2 f = __bfloat1622float2(bq);
-                        qf[nt][ks][e] = pack2<__half>(f.x, f.y);
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
-        }
-    }
     // causal limit (inclusive) of the query columns this thread accumulates
     int lim[NT][2];
 #pragma unroll
@@ -476,33 +477,63 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
             }
     }
     __syncthreads();
-
-    const bool direct = nparts == 1 && p.part0 == 0;
-    for (int idx = threadIdx.x; idx < p.rows * (D / 2); idx += blockDim.x) {
-        const int r = idx / (D / 2);
-        const int dp = (idx - r * (D / 2)) * 2;
+    // per row: the running max over the warps, each warp's factor 2^(m_w - M) and the row sum, once
+    float *wsc = mlw + DECODE_WARPS * RP * 2;           // [RP][DECODE_WARPS] factors, then [RP][2] (M, sum)
+    float *rml = wsc + RP * DECODE_WARPS;
+    for (int r = threadIdx.x; r < p.rows; r += blockDim.x) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < DECODE_WARPS; ++w) M = fmaxf(M, mlw[(w * RP + r) * 2]);
         const float Muse = M == -INFINITY ? 0.f : M;
-        float o0 = 0.f, o1 = 0.f, ls = 0.f;
+        float ls = 0.f;
 #pragma unroll
         for (int w = 0; w < DECODE_WARPS; ++w) {
             const float sc = exp2f(mlw[(w * RP + r) * 2] - Muse);
-            const float2 ov = *reinterpret_cast<const float2 *>(ow + (w * RP + r) * OSTR + dp);
-            o0 += sc * ov.x;
-            o1 += sc * ov.y;
+            wsc[r * DECODE_WARPS + w] = sc;
             ls += sc * mlw[(w * RP + r) * 2 + 1];
+        }
+        rml[r * 2] = M;
+        rml[r * 2 + 1] = ls;
+    }
+    __syncthreads();
+
+    // 8 dims of one row per thread and step (out is 16-byte aligned: every entry point checks it)
+    const bool direct = nparts == 1 && p.part0 == 0;
+    constexpr int D8 = D / 8;
+    for (int idx = threadIdx.x; idx < p.rows * D8; idx += blockDim.x) {
+        const int r = idx / D8;
+        const int d0 = (idx - r * D8) * 8;
+        const float M = rml[r * 2], ls = rml[r * 2 + 1];
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int w = 0; w < DECODE_WARPS; ++w) {
+            const float sc = wsc[r * DECODE_WARPS + w];
+            const float4 a = *reinterpret_cast<const float4 *>(ow + (w * RP + r) * OSTR + d0);
+            const float4 c = *reinterpret_cast<const float4 *>(ow + (w * RP + r) * OSTR + d0 + 4);
+            acc[0] += sc * a.x;
+            acc[1] += sc * a.y;
+            acc[2] += sc * a.z;
+            acc[3] += sc * a.w;
+            acc[4] += sc * c.x;
+            acc[5] += sc * c.y;
+            acc[6] += sc * c.z;
+            acc[7] += sc * c.w;
         }
         const int qi = r / p.G;
         const int h = g * p.G + (r - qi * p.G);
         const int64_t orow = ((int64_t)b * p.q_len + qi) * p.Hq + h;
         if (direct) {
-            *reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.out) + orow * D + dp) = pack2<T>(o0 / ls, o1 / ls);
+            *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + orow * D + d0) =
+                make_uint4(pack2<T>(acc[0] / ls, acc[1] / ls), pack2<T>(acc[2] / ls, acc[3] / ls),
+                           pack2<T>(acc[4] / ls, acc[5] / ls), pack2<T>(acc[6] / ls, acc[7] / ls));
         } else {
             const int64_t prow = orow * p.max_parts + part;
-            *reinterpret_cast<float2 *>(p.part_o + prow * D + dp) = make_float2(o0, o1);
-            if (dp == 0) p.part_ml[prow] = make_float2(M, ls);
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + d0);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (d0 == 0) p.part_ml[prow] = make_float2(M, ls);
         }
     }
 }
