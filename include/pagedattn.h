@@ -285,7 +285,8 @@ pa_status pa_copy_blocks(pa_pool *pool, const int32_t *pairs, int32_t n, void *k
  *   u      device fp32 [num_seqs, num_draft]  uniforms in [0, 1) for the accept tests
  *   v      device fp32 [num_seqs]              uniforms in [0, 1) for the final draw
  *   out    device int32 [num_seqs, num_draft + 1]  kept drafts, then the drawn token, then -1
- *   n_out  device int32 [num_seqs]             tokens emitted (kept drafts + 1)
+ *   n_out  device int32 [num_seqs]             tokens emitted (kept drafts + 1); 0 if the rows
+ *          could not be read (a bounded wait on a copy ran out), out[b] then holds no drawn token
  * num_draft <= 64. No pool is needed.
  */
 pa_status pa_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
