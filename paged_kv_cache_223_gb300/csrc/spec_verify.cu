@@ -6,16 +6,21 @@
 //
 // One CTA of 16 warps per sequence. Warp 0 runs the K accept tests in parallel (fp32: u * q < p) and
 // takes the first failure. The draw is an inverse CDF over the vocabulary in three levels:
-//   1. the row is cut into 256 segments of whole 128-value chunks; each warp sums 16 consecutive
-//      segments with coalesced float4 loads (eight chunks in flight per lane) into shared memory;
+//   1. the row is cut into 256 segments of whole 512-value chunks; each warp sums 16 consecutive
+//      segments into shared memory, streaming them through its own ring of three stages filled by
+//      1-D bulk copies (rows that are not 16-byte aligned: coalesced float4 loads, eight 128-value
+//      chunks in flight per lane, segments of whole 128-value chunks);
 //   2. warp 0 scans the 256 segment sums and finds the first segment whose running sum passes
 //      v * total;
-//   3. warp 0 walks that segment 512 values at a time (16 per lane: lane sums, an ordered warp scan,
-//      then the one lane where the running sum passes the target walks its values) to the token.
+//   3. warp 0 walks that segment 512 values at a time (16 per lane: lane sums and an ordered warp
+//      scan; the lane where the running sum passes the target spreads its 16 values over 16 lanes
+//      for a second scan) to the token.
 // Sums are double-single (a float pair hi + lo: Knuth's two-sum, Dekker's fast two-sum, and the
 // compensated sum of Ogita, Rump and Oishi within a lane), about 44 significant bits: near the fp64
-// sums of the definition at the fp32 rate, as fp64 arithmetic is scarce on this part. A weight
-// max(0, p - q) is formed exactly by a two-sum. A token is only ever drawn where its weight is > 0.
+// sums of the definition at the fp32 rate, as fp64 arithmetic is scarce on this part; comparisons
+// with the target are exact comparisons of normalised pairs. A weight max(0, p - q) is formed
+// exactly (Dekker's fast two-sum, exact whenever p >= q >= 0). A token is only ever drawn where its
+// weight is > 0.
 #include "pa_device.cuh"
 
 namespace pa {
