@@ -277,11 +277,24 @@ static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_
 // When the (sequence, KV head) units alone fill several waves of CTAs and a context spans only a few
 // partitions, splitting buys no parallelism and costs the partials and the merge launch: decode each
 // context as one partition.
+// Partitions per CTA, chosen at launch: all of them when the (sequence, KV head) units alone fill
+// three waves and contexts span at most 4 partitions; else the largest power of two that still
+// leaves at least 8 waves of CTAs (2 per SM) for the longest context. Fewer, longer partitions
+// write and merge fewer partial states and spread each CTA's fixed costs over more tiles.
 static void unsplit_if_filled(const pa_pool *pool, DecodeParams &p) {
     const int64_t units = (int64_t)p.num_seqs * p.Hkv;
-    if (p.max_parts > 1 && p.max_parts <= 4 && units >= 6LL * pool->sm_count) {
+    if (p.max_parts <= 1) return;
+    if (p.max_parts <= 4 && units >= 6LL * pool->sm_count) {
         p.part_tokens = p.max_parts * p.part_tokens;
         p.max_parts = 1;
+        return;
+    }
+    const int64_t want = 8LL * 2 * pool->sm_count;
+    int k = 1;
+    while (2 * k <= p.max_parts && units * ((p.max_parts + 2 * k - 1) / (2 * k)) >= want) k *= 2;
+    if (k > 1) {
+        p.part_tokens *= k;
+        p.max_parts = (p.max_parts + k - 1) / k;
     }
 }
 
