@@ -70,11 +70,13 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# sources that decide a kernel's DRAM traffic: the kernel, its helpers and, where the host picks the
+# launch shape (partitions per CTA, row tiles), the entry points
 TRAFFIC_SOURCES = {
-    "decode": ("decode.cu", "pa_device.cuh", "pa_internal.h"),
+    "decode": ("decode.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"),
     "spec": ("spec_verify.cu", "pa_device.cuh", "pa_internal.h"),
     "cow": ("copy_blocks.cu", "pa_device.cuh", "pa_internal.h"),
-    "prefill": ("prefill.cu", "pa_device.cuh", "pa_internal.h"),
+    "prefill": ("prefill.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"),
 }
 
 
