@@ -95,6 +95,24 @@ def test_edge_cases(case):
     H.assert_close(out, ref, f"edge {case}")
 
 
+def test_coarsened_partitions_every_sequence():
+    """Enough (sequence, KV head) units that the launch merges 512-token partitions in pairs (on a
+    152-SM part: 320 units x 8 merged partitions >= 8 waves of 2 CTAs per SM), with contexts on and
+    around the merged and unmerged partition edges and one at the table's maximum; every sequence
+    is checked against the oracle."""
+    edges = []
+    for c in range(1, 8):
+        edges += [1024 * c - 1, 1024 * c, 1024 * c + 1, 1024 * c + 512, 1024 * c - 511]
+    rng = np.random.default_rng(77)
+    lens = edges + [8192, 1, 16, 17] + [int(x) for x in rng.integers(1, 8193, size=160 - len(edges) - 4)]
+    wl = synth.custom_workload(lens, 16, 2, 64, 16, 1, synth.FP16, tag=260)
+    pool, kc, vc, q, tables, lens_d = H.build_device(wl)
+    out = pool.decode(q, tables, lens_d, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _, _ = H.oracle_reference(wl, 0)
+    H.assert_close(out, ref, "coarsened partitions")
+
+
 @pytest.mark.parametrize("stress", ["vmean", "qx8"])
 def test_stress_variants(stress):
     """Same shapes, harder numerics: V with mean 1 (relative tolerance governs) and q x 8 (peaked softmax)."""
