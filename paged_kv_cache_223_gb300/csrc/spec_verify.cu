@@ -12,9 +12,9 @@
 //      chunks in flight per lane, segments of whole 128-value chunks);
 //   2. warp 0 scans the 256 segment sums and finds the first segment whose running sum passes
 //      v * total;
-//   3. warp 0 walks that segment 512 values at a time (16 per lane: lane sums and an ordered warp
-//      scan; the lane where the running sum passes the target spreads its 16 values over 16 lanes
-//      for a second scan) to the token.
+//   3. the whole CTA walks that segment 512 values at a time, one value per thread (a warp scan, a
+//      scan of the 16 warp sums), and the first value whose running sum passes the target is the
+//      token.
 // Sums are double-single (a float pair hi + lo: Knuth's two-sum, Dekker's fast two-sum, and the
 // compensated sum of Ogita, Rump and Oishi within a lane), about 44 significant bits: near the fp64
 // sums of the definition at the fp32 rate, as fp64 arithmetic is scarce on this part; comparisons
@@ -149,13 +149,6 @@ __device__ __forceinline__ void load4(const SpecRow &r, int64_t i, int64_t end, 
     }
 }
 
-__device__ __forceinline__ void weights4(const float4 &a, const float4 &c, bool residual, DSum (&w)[4]) {
-    w[0] = weight(a.x, c.x, residual);
-    w[1] = weight(a.y, c.y, residual);
-    w[2] = weight(a.z, c.z, residual);
-    w[3] = weight(a.w, c.w, residual);
-}
-
 // Level 1 from shared memory: each warp streams its span through a private ring of SPEC_NS stages
 // filled by 1-D bulk copies (512 values of p, and of q for the residual, per stage). Returns false
 // when a copy never completed within the limit (after waiting, bounded, for the copies in flight).
@@ -278,6 +271,8 @@ __global__ void __launch_bounds__(SPEC_THREADS, 1) spec_verify_kernel(const floa
     __shared__ DSum s_before;
     __shared__ DSum s_target;
     __shared__ int s_rej, s_sel, s_abort;
+    __shared__ DSum s_wsum[SPEC_WARPS], s_wpre[SPEC_WARPS], s_btotal;
+    __shared__ int s_hit, s_last;
     const int64_t b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *o = out + b * (K + 1);
@@ -405,81 +400,56 @@ __global__ void __launch_bounds__(SPEC_THREADS, 1) spec_verify_kernel(const floa
         __syncthreads();
     }
 
-    // level 3: walk the chosen segment in blocks of 512 values, 16 consecutive values per lane: lane sums,
-    // one ordered warp scan, and the lane where the running sum passes the target walks its 16 values
-    if (warp == 0) {
-        const int sel = s_sel;
-        int tok = -1;
-        if (sel >= 0) {
-            const DSum target = s_target;
-            const int64_t s0 = sel * seg_len;
-            const int64_t s1 = s0 + seg_len < V ? s0 + seg_len : V;
-            DSum run = s_before;
-            int64_t last = -1;
-            for (int64_t blk = s0; blk < s1 && tok < 0; blk += 512) {
-                const int64_t i0 = blk + lane * 16;
-                DSum w[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float4 a, c;
-                    load4(row, i0 + 4 * j, s1, a, c);
-                    DSum w4[4];
-                    weights4(a, c, row.residual, w4);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) w[4 * j + e] = w4[e];
-                }
-                DSum t8[8], t4[4];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) t8[k] = ds_add(w[2 * k], w[2 * k + 1]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) t4[k] = ds_add(t8[2 * k], t8[2 * k + 1]);
-                const DSum mine = ds_add(ds_add(t4[0], t4[1]), ds_add(t4[2], t4[3]));
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (w[e].hi > 0.f) last = i0 + e;
-                DSum incl, excl;
-                warp_scan(mine, lane, incl, excl);
-                const unsigned hit = __ballot_sync(0xffffffffu, mine.hi > 0.f && ds_gt(ds_add(run, incl), target));
-                if (hit) {
-                    // spread lane fl's 16 values over lanes 0..15 and scan them from its running sum
-                    const int fl = __ffs(hit) - 1;
-                    DSum we{0.f, 0.f};
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const DSum x = shfl_ds(w[e], fl);
-                        if (lane == e) we = x;
-                    }
-                    DSum ie = we;
-#pragma unroll
-                    for (int d = 1; d < 16; d <<= 1) {
-                        const DSum up = shfl_up_ds(ie, d);
-                        if (lane >= d) ie = ds_add(up, ie);
-                    }
-                    const DSum base = shfl_ds(ds_add(run, excl), fl);
-                    const bool pos = lane < 16 && we.hi > 0.f;
-                    const unsigned pass = __ballot_sync(0xffffffffu, pos && ds_gt(ds_add(base, ie), target));
-                    const unsigned posm = __ballot_sync(0xffffffffu, pos);
-                    // the first value passing the target, else (rounding) the lane's last positive value
-                    const int e = pass ? __ffs(pass) - 1 : 31 - __clz(posm);
-                    tok = (int)(__shfl_sync(0xffffffffu, i0, fl) + e);
-                } else {
-                    run = ds_add(run, shfl_ds(incl, 31));
-                }
-            }
-            if (tok < 0) {
-                // the walk's sums fell short of the target by rounding: the segment's last positive token
-#pragma unroll
-                for (int m = 16; m > 0; m >>= 1) {
-                    const int64_t other = __shfl_xor_sync(0xffffffffu, last, m);
-                    last = other > last ? other : last;
-                }
-                tok = (int)last;
-            }
+    // level 3: the chosen segment, SPEC_THREADS values at a time, one per thread: a warp scan, a scan
+    // of the warp sums, and the first value whose running sum passes the target (else, after rounding,
+    // the segment's last value of positive weight)
+    const int sel = s_sel;
+    int tok = -1;
+    if (sel >= 0) {
+        const DSum target = s_target;
+        const int64_t s0 = sel * seg_len;
+        const int64_t s1 = s0 + seg_len < V ? s0 + seg_len : V;
+        DSum before = s_before;
+        if (tid == 0) {
+            s_hit = 0x7fffffff;
+            s_last = -1;
         }
-        if (lane == 0) {
-            o[n_kept] = tok;
-            n_out[b] = n_kept + 1;
+        for (int64_t blk = s0; blk < s1; blk += SPEC_THREADS) {
+            const int64_t i = blk + tid;
+            const DSum w = i < s1 ? weight(__ldg(row.p + i), row.residual ? __ldg(row.q + i) : 0.f, row.residual)
+                                  : DSum{0.f, 0.f};
+            DSum incl, excl;
+            warp_scan(w, lane, incl, excl);
+            if (lane == 31) s_wsum[warp] = incl;
+            __syncthreads();
+            if (warp == 0) {
+                const DSum x = lane < SPEC_WARPS ? s_wsum[lane] : DSum{0.f, 0.f};
+                DSum wi, we;
+                warp_scan(x, lane, wi, we);
+                if (lane < SPEC_WARPS) s_wpre[lane] = we;
+                if (lane == SPEC_WARPS - 1) s_btotal = wi;
+            }
+            __syncthreads();
+            const bool pos = w.hi > 0.f;
+            const bool hit = pos && ds_gt(ds_add(ds_add(before, s_wpre[warp]), incl), target);
+            const unsigned hb = __ballot_sync(0xffffffffu, hit), pb = __ballot_sync(0xffffffffu, pos);
+            if (lane == 0) {
+                if (hb) atomicMin(&s_hit, warp * 32 + __ffs(hb) - 1);
+                if (pb) atomicMax(&s_last, (int)(blk - s0) + warp * 32 + 31 - __clz(pb));
+            }
+            __syncthreads();
+            if (s_hit != 0x7fffffff) {
+                tok = (int)(blk + s_hit);
+                break;
+            }
+            before = ds_add(before, s_btotal);
+            __syncthreads();                             // s_wsum, s_wpre, s_btotal are rewritten next
         }
+        if (tok < 0 && s_last >= 0) tok = (int)(s0 + s_last);   // the running sums fell short by rounding
+    }
+    if (tid == 0) {
+        o[n_kept] = tok;
+        n_out[b] = n_kept + 1;
     }
 }
 
