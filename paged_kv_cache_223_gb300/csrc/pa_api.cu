@@ -281,7 +281,7 @@ static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_
 // three waves and contexts span at most 4 partitions; else the largest power of two that still
 // leaves at least 8 waves of CTAs (2 per SM) for the longest context. Fewer, longer partitions
 // write and merge fewer partial states and spread each CTA's fixed costs over more tiles.
-static void unsplit_if_filled(const pa_pool *pool, DecodeParams &p) {
+static void coarsen_partitions(const pa_pool *pool, DecodeParams &p) {
     const int64_t units = (int64_t)p.num_seqs * p.Hkv;
     if (p.max_parts <= 1) return;
     if (p.max_parts <= 4 && units >= 6LL * pool->sm_count) {
@@ -303,7 +303,7 @@ int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int3
     if (!pool) return -1;
     DecodeParams p;
     if (decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p) != PA_OK) return -1;
-    unsplit_if_filled(pool, p);
+    coarsen_partitions(pool, p);
     return p.max_parts > 1 ? 2 : 1;
 }
 
@@ -322,7 +322,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     DecodeParams p;
     pa_status st = decode_params(pool, block_table_stride, num_seqs, num_q_heads, q_len, p);
     if (st != PA_OK) return st;
-    unsplit_if_filled(pool, p);
+    coarsen_partitions(pool, p);
     p.q = q;
     p.out = out;
     p.block_tables = block_tables;
