@@ -62,7 +62,9 @@ def _check(p, q, draft, u, v):
 
 
 @pytest.mark.parametrize("B,K,V,agree", [(64, 5, 1000, 0.0), (64, 5, 1000, 0.9), (7, 1, 3, 0.5), (16, 0, 50, 0.0),
-                                         (32, 4, 128256, 0.8)])
+                                         (32, 4, 128256, 0.8),
+                                         (16, 40, 1000, 0.98),   # accept tests past the first 32 drafts
+                                         (8, 2, 1, 0.0)])        # one-token vocabulary
 def test_matches_oracle(B, K, V, agree):
     _check(*_case(B * 1000 + K + V, B, K, V, agree))
 
