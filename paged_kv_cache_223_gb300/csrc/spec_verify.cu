@@ -462,13 +462,10 @@ cudaError_t launch_spec_verify(const float *p, const float *q, const int32_t *dr
         spec_verify_kernel<false><<<B, SPEC_THREADS, 0, stream>>>(p, q, draft, u, v, K, V, out, n_out, status);
         return cudaGetLastError();
     }
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(spec_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)SPEC_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    // set on every call: the attribute belongs to the current device, and callers may use several
+    const cudaError_t e =
+        cudaFuncSetAttribute(spec_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPEC_SMEM);
+    if (e != cudaSuccess) return e;
     spec_verify_kernel<true><<<B, SPEC_THREADS, SPEC_SMEM, stream>>>(p, q, draft, u, v, K, V, out, n_out, status);
     return cudaGetLastError();
 }
