@@ -152,11 +152,48 @@ class Pool:
         except Exception:
             pass
 
+    def _check_caches(self, k_cache: Optional[torch.Tensor], v_cache: Optional[torch.Tensor]) -> None:
+        """Caches passed per call replace the pool's own: both or neither, each of the pool's shape."""
+        if (k_cache is None) != (v_cache is None):
+            raise ValueError("pass both k_cache and v_cache, or neither")
+        if k_cache is not None:
+            for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+                _dev(t, name, self.k_cache.dtype)
+                if tuple(t.shape) != tuple(self.k_cache.shape):
+                    raise ValueError(f"{name} must have shape {tuple(self.k_cache.shape)}")
+
+    def _attn_args(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                   out: Optional[torch.Tensor]) -> torch.Tensor:
+        """Checks the shapes the library trusts (it sees only pointers) and returns out."""
+        _dev(q, "q", self.dtype)
+        _dev(block_tables, "block_tables", torch.int32)
+        _dev(context_lens, "context_lens", torch.int32)
+        d = self.geometry[3]
+        if q.dim() != 4 or q.shape[3] != d:
+            raise ValueError(f"q must be [B, q_len, Hq, {d}], got {tuple(q.shape)}")
+        B = q.shape[0]
+        if block_tables.dim() != 2 or block_tables.shape[0] < B:
+            raise ValueError(f"block_tables must be [>= {B}, stride], got {tuple(block_tables.shape)}")
+        if context_lens.dim() != 1 or context_lens.shape[0] < B:
+            raise ValueError(f"context_lens must hold {B} entries, got {tuple(context_lens.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        _dev(out, "out", self.dtype)
+        if tuple(out.shape) != tuple(q.shape):
+            raise ValueError(f"out must have q's shape {tuple(q.shape)}, got {tuple(out.shape)}")
+        return out
+
     def cache_write(self, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                     k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
                     stream: Optional[torch.cuda.Stream] = None) -> None:
         """Scatter k, v [N, Hkv, d] into the slots given by slot_mapping (int64 [N]; -1 = skip)."""
         _dev(k, "k", self.dtype), _dev(v, "v", self.dtype), _dev(slot_mapping, "slot_mapping", torch.int64)
+        hd = (self.geometry[1], self.geometry[3])
+        if k.dim() != 3 or tuple(k.shape[1:]) != hd or tuple(v.shape) != tuple(k.shape):
+            raise ValueError(f"k and v must be [N, {hd[0]}, {hd[1]}], got {tuple(k.shape)} and {tuple(v.shape)}")
+        if slot_mapping.dim() != 1 or slot_mapping.shape[0] != k.shape[0]:
+            raise ValueError(f"slot_mapping must be [{k.shape[0]}], got {tuple(slot_mapping.shape)}")
+        self._check_caches(k_cache, v_cache)
         _check(lib().pa_cache_write(self.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.numel(),
                                     _ptr(k_cache), _ptr(v_cache), _stream(stream)), "pa_cache_write")
 
@@ -164,13 +201,9 @@ class Pool:
                out: Optional[torch.Tensor] = None, k_cache: Optional[torch.Tensor] = None,
                v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """Paged attention for q [B, q_len, Hq, d] -> out [B, q_len, Hq, d] (causal over the q_len rows)."""
-        _dev(q, "q", self.dtype)
-        _dev(block_tables, "block_tables", torch.int32)
-        _dev(context_lens, "context_lens", torch.int32)
+        out = self._attn_args(q, block_tables, context_lens, out)
+        self._check_caches(k_cache, v_cache)
         B, q_len, Hq, d = q.shape
-        if out is None:
-            out = torch.empty_like(q)
-        _dev(out, "out", self.dtype)
         _check(lib().pa_decode(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
                                _stream(stream)), "pa_decode")
@@ -181,13 +214,9 @@ class Pool:
                              k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
                              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """pa_decode_shared_prefix: decode for sequences whose tables share their first prefix_tokens tokens."""
-        _dev(q, "q", self.dtype)
-        _dev(block_tables, "block_tables", torch.int32)
-        _dev(context_lens, "context_lens", torch.int32)
+        out = self._attn_args(q, block_tables, context_lens, out)
+        self._check_caches(k_cache, v_cache)
         B, q_len, Hq, d = q.shape
-        if out is None:
-            out = torch.empty_like(q)
-        _dev(out, "out", self.dtype)
         _check(lib().pa_decode_shared_prefix(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                              block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale),
                                              int(prefix_tokens), _ptr(out), _stream(stream)),
@@ -198,13 +227,9 @@ class Pool:
                 out: Optional[torch.Tensor] = None, k_cache: Optional[torch.Tensor] = None,
                 v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """Chunked prefill (pa_prefill): q [B, C, Hq, 128] is a chunk of C new tokens per sequence, causal."""
-        _dev(q, "q", self.dtype)
-        _dev(block_tables, "block_tables", torch.int32)
-        _dev(context_lens, "context_lens", torch.int32)
+        out = self._attn_args(q, block_tables, context_lens, out)
+        self._check_caches(k_cache, v_cache)
         B, q_len, Hq, d = q.shape
-        if out is None:
-            out = torch.empty_like(q)
-        _dev(out, "out", self.dtype)
         _check(lib().pa_prefill(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                 block_tables.shape[1], _ptr(context_lens), B, Hq, q_len, float(scale), _ptr(out),
                                 _stream(stream)), "pa_prefill")
@@ -251,8 +276,18 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                         P, P]
         L.pa_decode_noalloc.restype = C.c_int
         _noalloc_ready = True
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _dev(t, name, q.dtype)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(context_lens, "context_lens", torch.int32)
+    if k_cache.dim() != 4 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [num_blocks, Hkv, block_size, d]")
     NB, Hkv, bs, d = k_cache.shape
+    if q.dim() != 4 or q.shape[3] != d or tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"q and out must be [B, q_len, Hq, {d}], got {tuple(q.shape)} and {tuple(out.shape)}")
     B, q_len, Hq, _ = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] < B or context_lens.dim() != 1 or context_lens.shape[0] < B:
+        raise ValueError("block_tables must be [>= B, stride] and context_lens [>= B]")
     return L.pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, d, _PA_DTYPE[q.dtype],
                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, q_len,
                                float(scale), partition_tokens, _ptr(out), _stream(stream))
@@ -354,6 +389,9 @@ def copy_blocks(pool: "Pool", pairs: torch.Tensor, k_cache: Optional[torch.Tenso
                 v_cache: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
     """pa_copy_blocks: copy whole blocks pairs[i, 0] -> pairs[i, 1] (device int32 [n, 2])."""
     _dev(pairs, "pairs", torch.int32)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError(f"pairs must be [n, 2], got {tuple(pairs.shape)}")
+    pool._check_caches(k_cache, v_cache)
     _check(_alloc_lib().pa_copy_blocks(pool.handle, _ptr(pairs), pairs.shape[0], _ptr(k_cache), _ptr(v_cache),
                                        _stream(stream)), "pa_copy_blocks")
 
@@ -374,7 +412,13 @@ def spec_verify(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u: torch.
     for name, t, dt in (("p", p, torch.float32), ("q", q, torch.float32), ("draft", draft, torch.int32),
                         ("u", u, torch.float32), ("v", v, torch.float32)):
         _dev(t, name, dt)
+    if p.dim() != 3:
+        raise ValueError(f"p must be [B, K + 1, V], got {tuple(p.shape)}")
     B, K1, V = p.shape
+    for name, t, shape in (("q", q, (B, K1 - 1, V)), ("draft", draft, (B, K1 - 1)), ("u", u, (B, K1 - 1)),
+                           ("v", v, (B,))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
     out = torch.empty((B, K1), dtype=torch.int32, device=p.device)
     n_out = torch.empty((B,), dtype=torch.int32, device=p.device)
     _check(L.pa_spec_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), _ptr(v), B, K1 - 1, V, _ptr(out), _ptr(n_out),

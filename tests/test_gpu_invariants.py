@@ -138,3 +138,35 @@ def test_bounded_wait_times_out_and_context_survives():
     assert pool.check() == pa.PA_OK
     ref, _, _ = H.oracle_reference(wl, 0)
     H.assert_close(out, ref, "decode after a timed-out wait")
+
+
+def test_binding_rejects_inconsistent_shapes():
+    """The library sees only pointers; the binding refuses shapes that would make it read or write past a buffer."""
+    wl = synth.custom_workload([40, 50], 8, 2, 64, 16, 1, synth.FP16, tag=64)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    bad = [
+        dict(out=torch.empty((1,) + tuple(q.shape[1:]), dtype=q.dtype, device=q.device)),   # out smaller than q
+    ]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc, **kw)
+    with pytest.raises(ValueError):                                   # one context length for two sequences
+        pool.decode(q, tables, lens[:1], wl.scale, k_cache=kc, v_cache=vc)
+    with pytest.raises(ValueError):                                   # one table row for two sequences
+        pool.decode(q, tables[:1], lens, wl.scale, k_cache=kc, v_cache=vc)
+    with pytest.raises(ValueError):                                   # head dim other than the pool's
+        pool.decode(torch.zeros(q.shape[:3] + (128,), dtype=q.dtype, device=q.device), tables, lens, wl.scale)
+    with pytest.raises(ValueError):                                   # only one of the two caches
+        pool.decode(q, tables, lens, wl.scale, k_cache=kc)
+    k = torch.zeros((3, 2, 64), dtype=torch.float16, device=H.DEV)
+    with pytest.raises(ValueError):                                   # fewer slots than rows
+        pool.cache_write(k, k, torch.zeros(2, dtype=torch.int64, device=H.DEV))
+    p = torch.full((2, 3, 10), 0.1, device=H.DEV)
+    qd = torch.full((2, 1, 10), 0.1, device=H.DEV)                     # K = 1 draft where p implies 2
+    d = torch.zeros((2, 2), dtype=torch.int32, device=H.DEV)
+    u = torch.zeros((2, 2), device=H.DEV)
+    with pytest.raises(ValueError):
+        pa.spec_verify(p, qd, d, u, torch.zeros(2, device=H.DEV))
+    with pytest.raises(ValueError):                                   # pairs must be [n, 2]
+        pa.copy_blocks(pool, torch.zeros((4, 3), dtype=torch.int32, device=H.DEV))
+    assert pool.check() == pa.PA_OK
