@@ -814,14 +814,19 @@ def cpu_baseline(wl: synth.Workload, seconds: float):
     import oracle
     nseq = pick_nseq(wl, seconds)
     hk, hv, news, q = oracle_sample(wl, nseq)
+    # whole passes over the sample until the time budget is spent (a pass rewrites the same slots)
     t0 = time.perf_counter()
-    threads = oracle_step(wl, hk, hv, news, q, nseq)
+    reps = 0
+    while reps == 0 or time.perf_counter() - t0 < seconds:
+        threads = oracle_step(wl, hk, hv, news, q, nseq)
+        reps += 1
     dt = time.perf_counter() - t0
     nbytes, toks = sample_bytes(wl, nseq)
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    return {"value": round(reps * nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"layer 0, sequences 0..{nseq - 1} of {wl.name}: cache write of the newest tokens + fp64 "
-                      f"paged attention ({toks} KV tokens, {nbytes} algorithmic bytes) in {dt:.2f} s",
-            "kv_tokens_per_s": round(toks / dt, 1)}
+                      f"paged attention ({toks} KV tokens, {nbytes} algorithmic bytes per pass), {reps} passes "
+                      f"in {dt:.2f} s",
+            "kv_tokens_per_s": round(reps * toks / dt, 1)}
 
 
 def run_reference(args):
