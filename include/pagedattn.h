@@ -315,27 +315,32 @@ int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int3
  * budget, or a latency-critical loop that must not make cudaMalloc's
  * synchronising call. Such a caller cannot create a pool, because
  * pa_pool_create allocates the split workspace. This entry point takes the
- * pool geometry directly and keeps the split workspace in one static device
- * array of PA_NOALLOC_SCRATCH_BYTES, which every GPU that runs it holds from
- * its first call until the process exits. The pages have no counterpart to
- * this entry point; it computes what pa_decode computes, with the same kernels.
+ * pool geometry directly and keeps its scratch (a status word and the split
+ * workspace) in one static device array of PA_NOALLOC_SCRATCH_BYTES, which
+ * every GPU that runs it holds from its first call until the process exits.
+ * The pages have no counterpart to this entry point; it computes what
+ * pa_decode computes, with the same decode and merge kernels.
  *
  *  - Inputs and outputs are the caller's, with pa_decode's layouts and meaning;
  *    num_blocks .. dtype and partition_tokens (0 = 512) are as in pa_pool_config.
- *  - Scratch needed when P = ceil(block_table_stride * block_size /
- *    partition_tokens) > 1: num_seqs * q_len * num_q_heads * P * head_dim * 4
- *    bytes (rounded up to 256) plus num_seqs * q_len * num_q_heads * P * 8.
- *    A larger request returns PA_ERR_INVALID_ARG before anything is launched.
+ *  - Scratch needed: 256 bytes (the status word), plus, when P =
+ *    ceil(block_table_stride * block_size / partition_tokens) > 1,
+ *    num_seqs * q_len * num_q_heads * P * head_dim * 4 bytes (rounded up to
+ *    256) and num_seqs * q_len * num_q_heads * P * 8. A larger request returns
+ *    PA_ERR_INVALID_ARG before anything is launched.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
- *  - The first call on a device, made with that device current, looks up the
- *    array's device address once; make that first call before any stream
- *    capture.
+ *  - The first call in a device's context, made with that device current,
+ *    looks up the array's device address (again after the context is reset);
+ *    make that first call before any stream capture.
  *  - Every call shares the one array and leaves its contents behind. Each call
- *    writes every scratch slot before reading it, so nothing needs clearing,
- *    but calls that overlap on the GPU (e.g. on two streams) race on the array
- *    and must be ordered by the caller.
- *  - There is no status word: an out-of-range block id or context length is
- *    clamped (the kernel does not fault) but not reported.
+ *    clears the status word (cudaMemsetAsync) and writes every partition slot
+ *    before reading it; calls that overlap on the GPU (e.g. on two streams)
+ *    race on the array and must be ordered by the caller.
+ *  - There is no status word to read back. Instead, when the kernels flag
+ *    anything -- a copy wait that ran out (its outputs would be left unwritten)
+ *    or an out-of-range block id or context length (clamped, so the kernel
+ *    does not fault) -- the call's last kernel fills the whole of `out` with
+ *    NaN, so a failed call never returns stale or partial results as numbers.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

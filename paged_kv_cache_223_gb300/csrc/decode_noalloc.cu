@@ -12,40 +12,74 @@ using namespace pa;
 namespace {
 
 constexpr size_t SCRATCH_BYTES = PA_NOALLOC_SCRATCH_BYTES;
+constexpr size_t STATUS_BYTES = 256;   // the call's device status word, padded to keep the partials aligned
 
-// The split pass's workspace: partition outputs followed by the (max, sum) pairs.
-// Every call writes each slot it later reads, so nothing needs clearing between calls.
+// The call's status word (bytes 0..3), then the split pass's workspace: partition outputs followed by
+// the (max, sum) pairs. Every call clears the status word and writes each partial slot it later reads.
 static __device__ __align__(256) unsigned char g_scratch[SCRATCH_BYTES];
+
+// Driver entry points (through the runtime, so the library needs no -lcuda).
+template <typename F>
+F driver_fn(const char *name, unsigned version) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+    static PFN_cuCtxGetCurrent_v4000 fn = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+    return fn;
+}
+
+PFN_cuCtxGetId_v12000 ctx_id_fn() {
+    static PFN_cuCtxGetId_v12000 fn = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+    return fn;
+}
+
+// Unique id of the calling thread's current context (false if there is none yet).
+bool current_ctx_id(unsigned long long *id) {
+    auto cur = ctx_current_fn();
+    auto gid = ctx_id_fn();
+    CUcontext c = nullptr;
+    if (!cur || !gid || cur(&c) != CUDA_SUCCESS || !c) return false;
+    return gid(c, id) == CUDA_SUCCESS;
+}
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_mu;
-void *g_scratch_ptr[MAX_DEVICES] = {};
+struct ScratchAddr {
+    void *ptr = nullptr;
+    unsigned long long ctx = 0;
+};
+ScratchAddr g_addr[MAX_DEVICES];
 
-// Device address of g_scratch on the current device (looked up once per device). In host
-// code the name g_scratch is only a host-side stand-in, so it is never passed to a kernel.
+// Device address of g_scratch in the current context of `device` (the current device). In host
+// code the name g_scratch is only a host-side stand-in, so it is never passed to a kernel. The
+// address is looked up on the first call in a context and again whenever the context changes
+// (after cudaDeviceReset the module is loaded anew and the array may sit elsewhere).
 cudaError_t scratch_address(int device, void **out) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[device]) {
+    unsigned long long id = 0;
+    const bool have_id = current_ctx_id(&id);
+    ScratchAddr &a = g_addr[device];
+    if (!a.ptr || !have_id || a.ctx != id) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);   // makes the primary context current if needed
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[device] = p;
+        if (!current_ctx_id(&id)) return cudaErrorContextIsDestroyed;
+        a.ptr = p;
+        a.ctx = id;
     }
-    *out = g_scratch_ptr[device];
+    *out = a.ptr;
     return cudaSuccess;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
+    static PFN_cuTensorMapEncodeTiled_v12000 fn =
+        driver_fn<PFN_cuTensorMapEncodeTiled_v12000>("cuTensorMapEncodeTiled", 12000);
     return fn;
 }
 
@@ -63,6 +97,15 @@ bool encode(const void *cache, int num_blocks, int Hkv, int bs, int D, int dtype
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// With no status word to hand back, a call whose kernels flagged anything (a copy wait that ran
+// out, which leaves outputs unwritten, or an out-of-range block id or context length) marks its
+// whole output as NaN (the all-ones 16-bit word is a NaN in fp16 and in bf16).
+__global__ void poison_on_error_kernel(const int *status, uint4 *out, int64_t nvec) {
+    if (__ldcg(status) == 0) return;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+}
 
 }  // namespace
 
@@ -95,10 +138,10 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
     const int64_t max_parts = (max_ctx + partition_tokens - 1) / partition_tokens;
     if ((int64_t)num_seqs * num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     if (max_parts > 1 && merge_smem_bytes(G, (int)max_parts, head_dim) > MAX_SMEM_PER_CTA) return PA_ERR_UNSUPPORTED;
-    // scratch needed: per (output row, partition) head_dim floats plus one (max, sum) pair
+    // scratch needed: the status word, then per (output row, partition) head_dim floats plus one (max, sum) pair
     const int64_t slots = (int64_t)num_seqs * q_len * num_q_heads * max_parts;
     const int64_t o_bytes = ((slots * head_dim * 4 + 255) / 256) * 256;
-    const int64_t need = max_parts > 1 ? o_bytes + slots * 8 : 0;
+    const int64_t need = (int64_t)STATUS_BYTES + (max_parts > 1 ? o_bytes + slots * 8 : 0);
     if (need > (int64_t)SCRATCH_BYTES) return PA_ERR_INVALID_ARG;   // beyond PA_NOALLOC_SCRATCH_BYTES
 
     int device = -1;
@@ -110,15 +153,16 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
         !encode(v_cache, num_blocks, num_kv_heads, block_size, head_dim, dtype, &tmv))
         return PA_ERR_CUDA;
 
+    unsigned char *sbase = static_cast<unsigned char *>(scratch);
     DecodeParams p;
     p.q = q;
     p.out = out;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.k_scales = p.v_scales = nullptr;
-    p.part_o = static_cast<float *>(scratch);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<unsigned char *>(scratch) + o_bytes);
-    p.status = nullptr;   // no status word on this path: bad ids / lengths are still clamped, not reported
+    p.status = reinterpret_cast<int *>(sbase);
+    p.part_o = reinterpret_cast<float *>(sbase + STATUS_BYTES);
+    p.part_ml = reinterpret_cast<float2 *>(sbase + STATUS_BYTES + o_bytes);
     p.stride = block_table_stride;
     p.num_seqs = num_seqs;
     p.Hq = num_q_heads;
@@ -134,7 +178,12 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_ns = 2000000000ull;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return PA_ERR_CUDA;
     if (launch_decode(p, dtype, head_dim, tmk, tmv, s) != cudaSuccess) return PA_ERR_CUDA;
     if (max_parts > 1 && launch_merge(p, dtype, head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
-    return PA_OK;
+    const int64_t nvec = (int64_t)num_seqs * q_len * num_q_heads * head_dim * 2 / 16;
+    const int64_t blocks = (nvec + 255) / 256;
+    poison_on_error_kernel<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, s>>>(p.status,
+                                                                                     static_cast<uint4 *>(out), nvec);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
