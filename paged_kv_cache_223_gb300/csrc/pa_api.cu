@@ -274,22 +274,22 @@ static pa_status decode_params(const pa_pool *pool, int32_t stride, int32_t num_
     return PA_OK;
 }
 
-// When the (sequence, KV head) units alone fill several waves of CTAs and a context spans only a few
-// partitions, splitting buys no parallelism and costs the partials and the merge launch: decode each
-// context as one partition.
 // Partitions per CTA, chosen at launch: all of them when the (sequence, KV head) units alone fill
 // three waves and contexts span at most 4 partitions; else the largest power of two that still
 // leaves at least 8 waves of CTAs (2 per SM) for the longest context. Fewer, longer partitions
-// write and merge fewer partial states and spread each CTA's fixed costs over more tiles.
+// write and merge fewer partial states and spread each CTA's fixed costs over more tiles. The
+// persistent tensor-core kernel (one CTA per SM walking its items) needs only about 4 items per SM
+// for balance, and each item ends with an epilogue, so it takes the coarsest split that keeps those.
 static void coarsen_partitions(const pa_pool *pool, DecodeParams &p) {
     const int64_t units = (int64_t)p.num_seqs * p.Hkv;
     if (p.max_parts <= 1) return;
+    const bool persistent = decode_uses_verify(pool->cfg.head_dim, p.rows, pool->cfg.kv_format == PA_KV_FP8_E4M3);
     if (p.max_parts <= 4 && units >= 6LL * pool->sm_count) {
         p.part_tokens = p.max_parts * p.part_tokens;
         p.max_parts = 1;
         return;
     }
-    const int64_t want = 8LL * 2 * pool->sm_count;
+    const int64_t want = persistent ? 4LL * pool->sm_count : 8LL * 2 * pool->sm_count;
     int k = 1;
     while (2 * k <= p.max_parts && units * ((p.max_parts + 2 * k - 1) / (2 * k)) >= want) k *= 2;
     if (k > 1) {
@@ -340,6 +340,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     if ((st = tensor_map(pool, v_cache, &tmv)) != PA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, pool->cfg.head_dim, pool->sm_count);
+    p.vf_ctas = pool->sm_count;
     if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s, kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
@@ -392,6 +393,13 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
                 p.pchunk = k;
             }
         }
+    }
+    // a persistent suffix decode (the tensor-core kernel, for more than 8 rows per KV head) takes the SMs
+    // the prefix kernel leaves free, so that the two run side by side
+    {
+        const int64_t ctiles = (((int64_t)num_seqs * p.rows + 127) / 128 + 1) / 2;
+        const int64_t prefix_ctas = ctiles * p.Hkv * ((p.part0 + p.pchunk - 1) / p.pchunk);
+        p.vf_ctas = prefix_ctas < pool->sm_count ? (int)(pool->sm_count - prefix_ctas) : pool->sm_count;
     }
     // the prefix kernel (tensor cores, one CTA per SM) goes first, straight onto the caller's stream, so
     // that its CTAs take whole SMs before the suffix decode (bandwidth, many small CTAs, on the pool's

@@ -46,6 +46,7 @@ struct DecodeParams {
     int pchunk = 1;      // prefix partitions per prefix-kernel CTA (their combined state goes to the first)
     int merge_splits = 1;  // merge CTAs per (sequence, query position, KV head): each takes a share of
                            // the (row, 4-dim) columns, so small batches still fill the GPU
+    int vf_ctas = 0;       // tensor-core verify kernel: persistent CTAs (0 = one per SM of the device)
 };
 
 struct CacheWriteParams {
@@ -83,7 +84,13 @@ cudaError_t launch_prefill(const DecodeParams &p, int dtype, const CUtensorMap &
 // (blocks from sequence 0's table), written as partition partials for the merge.
 cudaError_t launch_prefix(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                           cudaStream_t stream);
+// Tensor-core decode of 9..32 query rows per KV head (16-bit pools, head_dim 128): persistent, at most
+// max_ctas CTAs (one per SM).
+cudaError_t launch_verify(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                          int max_ctas, cudaStream_t stream);
+bool decode_uses_verify(int head_dim, int rows, bool kv8);
 size_t decode_smem_bytes(int head_dim, int nt);
+size_t verify_smem_bytes();
 size_t prefill_smem_bytes();
 size_t merge_smem_bytes(int G, int max_parts, int head_dim, int splits = 1);
 int merge_splits_for(int64_t units, int G, int head_dim, int sm_count);

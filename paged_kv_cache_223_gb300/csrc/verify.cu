@@ -1,0 +1,651 @@
+// verify.cu -- paged attention for 9..32 query rows per KV head (a head group's speculative draft
+// rows, or a wide GQA group) on the 5th-generation tensor cores.
+//
+// What is computed is pa_decode's definition (learn.tanhdev.com "Part 8: Inference optimization
+// with vLLM", section on executing the kernel math in CUDA: A_{i,j} = q_i K_(j)^T / sqrt(d_k),
+// softmax across the blocks, o_i = sum_j sum_t a_{i,j,t} v_(j,t)), with the draft rows of a verify
+// pass (itimpress.au section 1: the target checks the K = 5 drafted tokens in one parallel pass;
+// yangyu.win blog #54 section 2.4) each seeing the context up to its own position. Work items are
+// the decode's (sequence, KV head, context partition) triples, so partial states and the
+// log-sum-exp merge are shared with decode.cu.
+//
+// Per 128-key tile, with the query rows on the M side (row r of a copy in tensor-memory lane r of
+// that copy's quarter):
+//   S [128 x 128 keys] = Q4 [128 x 128 d] . K_tile^T   (M128 N128 K16 x 8; Q4 in tensor memory)
+//   O [128 x 128 d]   += P4 [128 x 128 keys] . V_tile   (M128 N128 K16 x 8; P4 in tensor memory)
+// Q4 holds four copies of the head group's (up to 32) query rows, one per 32-lane quarter, so that
+// all four sub-partitions of the SM take part in the softmax (a warp reaches only its own quarter,
+// and an exponential costs the same per warp instruction however many lanes are active). Each copy
+// owns a slice of every tile's keys and runs its own online softmax over that slice (its own running
+// max and sum); its weights outside the slice are zero, so its O rows accumulate only its slice. The
+// epilogue merges the copies with the log-sum-exp rule. fp16: four slices of 32 keys. bf16: two
+// slices of 64 keys, each held by two copies, one writing the weights' high parts (bf16(p)) and one
+// the low parts (bf16(p - hi)), so that P keeps 16 significant bits (8 alone fail the tolerance
+// where weighted values cancel) with no extra tensor-core work. K and V tiles are read from shared
+// memory once per tile each; Q and P never touch it.
+//
+// One persistent CTA per SM walks its items (c, c + grid, ...); every role follows the same
+// sequence of tiles, so the copies of the next item start while the current one finishes.
+//   warps 0-3   softmax of copy w (quarter w), then the epilogue: copies merged through shared memory,
+//               rows normalised and stored.
+//   warp 4      MMA issue (one thread) and tensor-memory allocation.
+//   warps 8-11  K producers, warps 12-15 V producers: each warp copies two 16-key sub-tiles of every
+//               tile, one TMA box per 64-dimension half; block ids looked up one tile ahead (one warp's
+//               copies are issued one after another, and TMA throughput scales with issuing warps).
+//               The K producer of quarter q also writes the item's query rows into Q4's quarter q.
+// Every wait is bounded and abortable; a timeout sets the status word, the CTA drains its copies
+// and MMAs, frees tensor memory and returns without writing results.
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int VF_KT = 128;                             // keys per tile
+constexpr int VF_D = 128;                              // head dimension
+constexpr int VF_ROWS = 32;                            // query rows per KV head, at most
+constexpr int VF_KSTAGES = 3, VF_VSTAGES = 2;
+constexpr int VF_TILE_BYTES = VF_KT * VF_D * 2;        // 32 KB: K or V tile, [2 halves][128 keys][128 B]
+constexpr int VF_HALF_BYTES = VF_KT * 128;             // 16 KB
+constexpr int VF_ST_STRIDE = VF_D + 4;                 // fp32 staging row (padded: no bank conflicts)
+constexpr int VF_OFF_K = 0;
+constexpr int VF_OFF_V = VF_OFF_K + VF_KSTAGES * VF_TILE_BYTES;
+constexpr int VF_OFF_ST = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;   // staging [2][32 rows][VF_ST_STRIDE] fp32
+constexpr int VF_OFF_ML = VF_OFF_ST + 2 * VF_ROWS * VF_ST_STRIDE * 4;  // (max, sum) per copy and row [4][32]
+constexpr int VF_OFF_BAR = VF_OFF_ML + 4 * VF_ROWS * 8;
+// barriers: k_full[3] k_empty[3] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
+//           o_full o_free ml st1 st2 drain
+constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6;
+constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4]
+constexpr int VF_SMEM = 1024 + VF_OFF_MISC + 64;
+static_assert(VF_OFF_BAR % 8 == 0, "barrier alignment");
+static_assert(VF_SMEM <= 227 * 1024, "verify shared memory");
+
+// 16 warps; warps 5-7 only take part in the prologue and teardown. Launched at 128 registers per thread;
+// the softmax warpgroup raises its share and the other three lower theirs (setmaxnreg):
+// 128 x 232 + 384 x 88 <= 512 x 128.
+constexpr int VF_THREADS = 512;
+constexpr int VF_MMA_WARP = 4, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
+constexpr uint32_t VF_REGS_HIGH = 232, VF_REGS_LOW = 88;
+static_assert(128 * VF_REGS_HIGH + 384 * VF_REGS_LOW <= VF_THREADS * 128, "register split");
+// tensor memory: Q4[2] at columns 0 / 64 (128 d as 64 packed columns), S/P[2] at 128 / 256, O at 384
+constexpr uint32_t VF_TMEM_COLS = 512;
+constexpr uint32_t VF_COL_Q = 0, VF_COL_S = 128, VF_COL_O = 384;
+constexpr float VF_RESCALE_LOG2 = 8.f;                 // stale-max headroom (P <= 2^8)
+
+size_t verify_smem_bytes() { return VF_SMEM; }
+
+// Copies keep the normal L2 priority: blocks shared by several tables (a copy-on-write prefix) are read
+// again by other CTAs, other blocks once.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bounded wait that also gives up when another role has aborted the CTA. Roles that run ahead of the
+// others (copies, Q loads) pass a back-off: between polls they sleep instead of taking issue slots from
+// the softmax warps that share their sub-partitions.
+__device__ __forceinline__ bool vf_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort_flag,
+                                        uint32_t sleep_ns = 0) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (sleep_ns) __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 || sleep_ns) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+struct VfItem {
+    int idx;              // item index: (sequence, KV head, partition)
+    int b, g, part, L;
+    int t_begin, t_end;   // the item's tokens [t_begin, t_end): its partition, cut at the context end
+    int ntiles;
+};
+
+// The CTA's items (idx = blockIdx.x, + gridDim.x, ...) in order. The next item's context length is
+// loaded one item ahead, so that no role waits on that load at an item boundary.
+struct VfItems {
+    const DecodeParams &p;
+    int nlaunch, n_items, idx, Lnext;
+
+    __device__ __forceinline__ VfItems(const DecodeParams &p_, int nlaunch_, int n_items_)
+        : p(p_), nlaunch(nlaunch_), n_items(n_items_), idx(blockIdx.x) {
+        Lnext = idx < n_items ? __ldg(p.context_lens + idx / nlaunch / p.Hkv) : 0;
+    }
+
+    __device__ __forceinline__ bool next(VfItem &it) {
+        if (idx >= n_items) return false;
+        it.idx = idx;
+        it.part = p.part0 + idx % nlaunch;
+        const int bg = idx / nlaunch;
+        it.g = bg % p.Hkv;
+        it.b = bg / p.Hkv;
+        const int L = Lnext < 0 ? 0 : (Lnext > p.max_ctx ? p.max_ctx : Lnext);
+        it.L = L;
+        const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
+        it.t_begin = it.part * p.part_tokens;
+        if (it.part >= nparts) {
+            it.t_end = it.t_begin;
+            it.ntiles = 0;
+        } else {
+            it.t_end = min(it.t_begin + p.part_tokens, L);
+            it.ntiles = (it.t_end - it.t_begin + VF_KT - 1) / VF_KT;
+        }
+        idx += gridDim.x;
+        if (idx < n_items) Lnext = __ldg(p.context_lens + idx / nlaunch / p.Hkv);
+        return true;
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(VF_THREADS, 1)
+    verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeParams p) {
+    constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int NSLICE = SPLIT_P ? 2 : 4;              // key slices per tile
+    constexpr int SW = VF_KT / NSLICE;                    // keys per slice (32 or 64)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_u32);
+    const uint32_t bar_k_full = base + VF_OFF_BAR;
+    const uint32_t bar_k_empty = bar_k_full + VF_KSTAGES * 8;
+    const uint32_t bar_v_full = bar_k_empty + VF_KSTAGES * 8;
+    const uint32_t bar_v_empty = bar_v_full + VF_VSTAGES * 8;
+    const uint32_t bar_q_full = bar_v_empty + VF_VSTAGES * 8;
+    const uint32_t bar_q_free = bar_q_full + 16;
+    const uint32_t bar_s_full = bar_q_free + 16;
+    const uint32_t bar_p_full = bar_s_full + 16;
+    const uint32_t bar_pv_done = bar_p_full + 16;
+    const uint32_t bar_o_full = bar_pv_done + 16;
+    const uint32_t bar_o_free = bar_o_full + 8;
+    const uint32_t bar_ml = bar_o_free + 8;
+    const uint32_t bar_st1 = bar_ml + 8;
+    const uint32_t bar_st2 = bar_st1 + 8;
+    const uint32_t bar_drain = bar_st2 + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + VF_OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *issued = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [K warps 0..3, V warps 0..3]
+    float *stage = reinterpret_cast<float *>(smem + VF_OFF_ST);                // [2][32][VF_ST_STRIDE]
+    float2 *mlx = reinterpret_cast<float2 *>(smem + VF_OFF_ML);                // [4 copies][32 rows]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nlaunch = p.max_parts - p.part0;
+    const int n_items = p.num_seqs * p.Hkv * nlaunch;
+
+    // ---- prologue: barriers, tensor memory
+    if (warp == VF_MMA_WARP) tmem_alloc(smem_u32(tmem_slot), VF_TMEM_COLS);
+    if (tid == 0) {
+        for (int s = 0; s < VF_KSTAGES; ++s) {
+            mbar_init(bar_k_full + s * 8, 4);
+            mbar_init(bar_k_empty + s * 8, 1);
+        }
+        for (int s = 0; s < VF_VSTAGES; ++s) {
+            mbar_init(bar_v_full + s * 8, 4);
+            mbar_init(bar_v_empty + s * 8, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_q_full + s * 8, 128);
+            mbar_init(bar_q_free + s * 8, 1);
+            mbar_init(bar_s_full + s * 8, 1);
+            mbar_init(bar_p_full + s * 8, 128);
+            mbar_init(bar_pv_done + s * 8, 1);
+        }
+        mbar_init(bar_o_full, 1);
+        mbar_init(bar_o_free, 128);
+        mbar_init(bar_ml, 128);
+        mbar_init(bar_st1, 64);
+        mbar_init(bar_st2, 32);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        for (int i = 0; i < 8; ++i) issued[i] = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int consumed_k = 0, consumed_v = 0;   // MMA thread: tiles whose copies were seen to land
+
+    if (warp >= 4) {
+        setmaxnreg_dec<VF_REGS_LOW>();
+        if (warp >= VF_KPROD_WARP) {
+            // ------------------------------------------------------------------ K / V producers
+            const bool is_v = warp >= VF_VPROD_WARP;
+            const int pw = warp - (is_v ? VF_VPROD_WARP : VF_KPROD_WARP);   // also the tensor-memory quarter
+            const int NS = is_v ? VF_VSTAGES : VF_KSTAGES;
+            const uint32_t full0 = is_v ? bar_v_full : bar_k_full;
+            const uint32_t empty0 = is_v ? bar_v_empty : bar_k_empty;
+            const uint32_t ring = base + (is_v ? VF_OFF_V : VF_OFF_K);
+            const CUtensorMap *map = is_v ? &tmv : &tmk;
+            const int sub = 2 * pw + ((lane >> 1) & 1);   // lanes 0..3: two sub-tiles x two halves
+            const int h = lane & 1;
+            const uint64_t policy = l2_policy_evict_normal();
+            const uint32_t q_lane_base = (uint32_t)(pw * 32) << 16;
+            const int qn = lane, qqi = qn < p.rows ? qn / p.G : 0, qhh = qn - qqi * p.G;
+            int jj = 0, ii = 0;
+            bool ok = true;
+            VfItems items(p, nlaunch, n_items);
+            VfItem it;
+            while (ok && items.next(it)) {
+                if (!is_v && pw == 0 && it.part == p.part0) {
+                    const int Lraw = __ldg(p.context_lens + it.b);
+                    if ((Lraw < p.q_len || Lraw > p.max_ctx) && lane == 0) set_status(p.status, STATUS_BOUNDS);
+                    if (p.part0 > 0 && it.g == 0) {
+                        // shared-prefix decode: the prefix kernel read sequence 0's blocks for every sequence and
+                        // assumed that every query row follows the whole prefix; check both for this sequence
+                        const int pre_blocks = p.part0 * p.part_tokens / p.bs;
+                        if (it.L - p.q_len < p.part0 * p.part_tokens && lane == 0) set_status(p.status, STATUS_BOUNDS);
+                        for (int i = lane; i < pre_blocks; i += 32)
+                            if (__ldg(p.block_tables + (int64_t)it.b * p.stride + i) != __ldg(p.block_tables + i))
+                                set_status(p.status, STATUS_BOUNDS);
+                    }
+                }
+                if (it.ntiles == 0) continue;
+                const int32_t *trow = p.block_tables + (int64_t)it.b * p.stride;
+                const int tok0 = it.t_begin + sub * TILE_TOKENS;      // this lane's sub-tile in tile 0
+                int id_next = (lane < 4 && tok0 < it.t_end) ? __ldg(trow + tok0 / p.bs) : 0;
+                if (!is_v) {
+                    // the item's query rows into quarter pw of Q4 (buffer ii & 1, free once the item two before
+                    // has had its last S)
+                    if (ii >= 2 &&
+                        !__all_sync(0xffffffffu, vf_wait(bar_q_free + (ii & 1) * 8, (uint32_t)((ii >> 1) - 1) & 1u,
+                                                         p.wait_ns, abort_flag, 256))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4 *qrow = reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const T *>(p.q) + (((int64_t)it.b * p.q_len + qqi) * p.Hq + it.g * p.G + qhh) * VF_D);
+                    const uint32_t qcol = tmem + q_lane_base + VF_COL_Q + (ii & 1) * 64;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 v = qn < p.rows ? __ldg(qrow + 8 * half + c) : make_uint4(0u, 0u, 0u, 0u);
+                            w[4 * c] = v.x;
+                            w[4 * c + 1] = v.y;
+                            w[4 * c + 2] = v.z;
+                            w[4 * c + 3] = v.w;
+                        }
+                        tmem_st32_raw(qcol + 32 * half, w);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar_q_full + (ii & 1) * 8);
+                }
+                ++ii;
+                for (int t = 0; t < it.ntiles; ++t, ++jj) {
+                    const int tok = tok0 + t * VF_KT;
+                    const bool valid = lane < 4 && tok < it.t_end;
+                    int id = id_next;
+                    // the block id of the next tile's sub-tile is loaded now, used one tile later
+                    if (t + 1 < it.ntiles && lane < 4 && tok + VF_KT < it.t_end) id_next = __ldg(trow + (tok + VF_KT) / p.bs);
+                    const int st = jj % NS;
+                    if (jj >= NS) {
+                        const bool got = vf_wait(empty0 + st * 8, (uint32_t)((jj / NS) - 1) & 1u, p.wait_ns, abort_flag, 256);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                    if (lane == 0) mbar_arrive_expect_tx(full0 + st * 8, (uint32_t)__popc(vmask) * (TILE_TOKENS * 128));
+                    __syncwarp();
+                    if (valid) {
+                        if (id < 0 || id >= p.num_blocks) {
+                            set_status(p.status, STATUS_BOUNDS);
+                            id = 0;
+                        }
+                        const int row0 = (id * p.Hkv + it.g) * p.bs + tok % p.bs;
+                        tma_load_2d(ring + st * VF_TILE_BYTES + h * VF_HALF_BYTES + sub * TILE_TOKENS * 128, map,
+                                    h * 64, row0, full0 + st * 8, policy);
+                    }
+                }
+            }
+            if (lane == 0) issued[(is_v ? 4 : 0) + pw] = jj;
+        } else if (warp == VF_MMA_WARP) {
+            // ------------------------------------------------------------------ MMA issue (lane 0)
+            if (lane == 0) {
+                const uint32_t idesc_s = umma_idesc<T>(128, VF_KT, false);
+                const uint32_t idesc_o = umma_idesc<T>(128, VF_D, true);
+                const uint64_t dk0 = umma_desc_sw128(base + VF_OFF_K, 16, 1024);
+                const uint64_t dv0 = umma_desc_sw128(base + VF_OFF_V, VF_HALF_BYTES, 1024);
+                bool ok = true;
+                int jj = 0, ii = 0;
+                int pv_jj = -1, pv_ii = 0;
+                bool pv_first = false, pv_last = false;
+                auto do_pv = [&]() -> bool {       // O += P(pv_jj) V(pv_jj)
+                    if (!vf_wait(bar_p_full + (pv_jj & 1) * 8, (uint32_t)(pv_jj >> 1) & 1u, p.wait_ns, abort_flag))
+                        return false;
+                    if (!vf_wait(bar_v_full + (pv_jj % VF_VSTAGES) * 8, (uint32_t)(pv_jj / VF_VSTAGES) & 1u, p.wait_ns,
+                                 abort_flag))
+                        return false;
+                    consumed_v = pv_jj + 1;
+                    // the item's first product overwrites O: the previous item's epilogue must have read it
+                    if (pv_first && pv_ii >= 1 &&
+                        !vf_wait(bar_o_free, (uint32_t)(pv_ii - 1) & 1u, p.wait_ns, abort_flag))
+                        return false;
+                    tc_fence_after();
+                    const uint64_t dv = dv0 + (uint64_t)(((pv_jj % VF_VSTAGES) * VF_TILE_BYTES) >> 4);
+                    const uint32_t pcol = tmem + VF_COL_S + (pv_jj & 1) * 128;
+#pragma unroll
+                    for (int ks = 0; ks < VF_KT / 16; ++ks)
+                        umma_f16_tmem_a(tmem + VF_COL_O, pcol + ks * 8, dv + (uint64_t)((ks * 16 * 128) >> 4), idesc_o,
+                                        (ks > 0 || !pv_first) ? 1u : 0u);
+                    umma_commit(bar_v_empty + (pv_jj % VF_VSTAGES) * 8);
+                    umma_commit(bar_pv_done + (pv_jj & 1) * 8);
+                    if (pv_last) umma_commit(bar_o_full);
+                    return true;
+                };
+                VfItems items(p, nlaunch, n_items);
+                VfItem it;
+                while (ok && items.next(it)) {
+                    if (it.ntiles == 0) continue;
+                    if (!(ok = vf_wait(bar_q_full + (ii & 1) * 8, (uint32_t)(ii >> 1) & 1u, p.wait_ns, abort_flag)))
+                        break;
+                    const uint32_t qcol = tmem + VF_COL_Q + (ii & 1) * 64;
+                    for (int t = 0; t < it.ntiles; ++t, ++jj) {
+                        if (!(ok = vf_wait(bar_k_full + (jj % VF_KSTAGES) * 8, (uint32_t)(jj / VF_KSTAGES) & 1u,
+                                           p.wait_ns, abort_flag)))
+                            break;
+                        consumed_k = jj + 1;
+                        tc_fence_after();
+                        // S(jj) = Q4 K(jj)^T over the S/P buffer of tile jj; it is issued after P(jj-2).V, which read
+                        // that buffer (one thread's MMAs execute in order)
+                        const uint64_t dk = dk0 + (uint64_t)(((jj % VF_KSTAGES) * VF_TILE_BYTES) >> 4);
+                        const uint32_t scol = tmem + VF_COL_S + (jj & 1) * 128;
+#pragma unroll
+                        for (int ks = 0; ks < VF_D / 16; ++ks)
+                            umma_f16_tmem_a(scol, qcol + ks * 8,
+                                            dk + (uint64_t)(((ks >> 2) * VF_HALF_BYTES + (ks & 3) * 32) >> 4), idesc_s,
+                                            ks > 0 ? 1u : 0u);
+                        umma_commit(bar_k_empty + (jj % VF_KSTAGES) * 8);
+                        umma_commit(bar_s_full + (jj & 1) * 8);
+                        if (t == it.ntiles - 1) umma_commit(bar_q_free + (ii & 1) * 8);
+                        if (pv_jj >= 0 && !(ok = do_pv())) break;
+                        pv_jj = jj;
+                        pv_ii = ii;
+                        pv_first = t == 0;
+                        pv_last = t == it.ntiles - 1;
+                    }
+                    ++ii;
+                }
+                if (ok && pv_jj >= 0) ok = do_pv();
+                if (!ok) *abort_flag = 1;
+            }
+            __syncwarp();
+        }
+    } else {
+        setmaxnreg_inc<VF_REGS_HIGH>();
+        // ---------------------------------------------------------------------- softmax + epilogue (copy `warp`)
+        const int slice = SPLIT_P ? (warp & 1) : warp;       // this copy's keys: [slice * SW, slice * SW + SW)
+        const bool lo_part = SPLIT_P && warp >= 2;           // writes the weights' low parts
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int n = lane;                                  // query row (of the head group)
+        const int qi = n < p.rows ? n / p.G : p.q_len - 1;
+        int jj = 0, ii = 0;
+        bool ok = true;
+        VfItems items(p, nlaunch, n_items);
+        VfItem it;
+        while (ok && items.next(it)) {
+            if (it.ntiles == 0) continue;
+            const int lim = it.L - p.q_len + qi;              // last key this row sees
+            float m_ref = -INFINITY, l = 0.f;
+            for (int t = 0; t < it.ntiles; ++t, ++jj) {
+                ok = __all_sync(0xffffffffu, vf_wait(bar_s_full + (jj & 1) * 8, (uint32_t)(jj >> 1) & 1u, p.wait_ns,
+                                                     abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t scol = tmem + lane_base + VF_COL_S + (jj & 1) * 128;
+                float sv[SW];
+                tmem_ld_cols<SW>(scol + slice * SW, sv);
+                const int t0 = it.t_begin + t * VF_KT;
+                const int k0 = t0 + slice * SW;               // absolute index of the slice's first key
+                const int nvalid = it.t_end - t0;             // keys of this tile inside the item (>= 1)
+                // last visible key of this row in the slice (keys past the item or the row's limit are masked)
+                const int cut = min(it.t_end - 1, lim) - k0;
+                float m4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m4[i] = -INFINITY;
+                if (cut >= SW - 1) {
+#pragma unroll
+                    for (int c = 0; c < SW; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < SW; ++c) {
+                        sv[c] = c <= cut ? sv[c] : -INFINITY;
+                        m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+                    }
+                }
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (mx > m_ref + VF_RESCALE_LOG2 || (m_ref == -INFINITY && mx > -INFINITY)) {
+                    alpha = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - mx);
+                    m_ref = mx;
+                    rescale = true;
+                }
+                if (t > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // O holds the item's P.V up to tile t-1: wait for that product, then rescale this copy's rows
+                    ok = __all_sync(0xffffffffu, vf_wait(bar_pv_done + ((jj - 1) & 1) * 8,
+                                                         (uint32_t)((jj - 1) >> 1) & 1u, p.wait_ns, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < VF_D; c0 += 32) {
+                        float a[32];
+                        tmem_ld32(tmem + lane_base + VF_COL_O + c0, a);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) a[c] *= alpha;
+                        tmem_st32(tmem + lane_base + VF_COL_O + c0, a);
+                    }
+                }
+                const float nmuse = m_ref == -INFINITY ? 0.f : -m_ref;
+                float r4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) r4[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < SW; ++c) {
+                    sv[c] = ex2_approx(fmaf(sv[c], p.scale_log2, nmuse));
+                    r4[c & 3] += sv[c];
+                }
+                l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+                // P4 row: 128 keys as 64 packed columns; this copy's slice holds its weights (the high or the low
+                // parts), the other slices zero
+                {
+                    uint32_t wv[SW / 2];
+#pragma unroll
+                    for (int c = 0; c < SW / 2; ++c) {
+                        const float x0 = sv[2 * c], x1 = sv[2 * c + 1];
+                        wv[c] = pack2<T>(x0, x1);
+                        if (lo_part) {
+                            // a bf16 is the top half of an fp32
+                            const float h0 = __uint_as_float(wv[c] << 16), h1 = __uint_as_float(wv[c] & 0xFFFF0000u);
+                            wv[c] = pack2<T>(x0 - h0, x1 - h1);
+                        }
+                    }
+                    // the slice's packed columns lie in 32-column group g (fp16: in its low or high half)
+                    const int g = (slice * (SW / 2)) >> 5;
+                    uint32_t w[32];
+                    if constexpr (SW / 2 == 32) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) w[c] = wv[c];
+                    } else {
+                        const bool upper = (slice & 1) != 0;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            w[c] = upper ? 0u : wv[c];
+                            w[16 + c] = upper ? wv[c] : 0u;
+                        }
+                    }
+                    tmem_st32_raw(scol + 32 * g, w);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) w[c] = 0u;
+                    tmem_st32_raw(scol + 32 * (1 - g), w);
+                }
+                if (nvalid < VF_KT && warp == 0) {
+                    // keys past the item: their V rows hold other data (possibly NaN): zero them once the tile has
+                    // landed, so that a zero weight times the row stays zero
+                    ok = __all_sync(0xffffffffu, vf_wait(bar_v_full + (jj % VF_VSTAGES) * 8,
+                                                         (uint32_t)(jj / VF_VSTAGES) & 1u, p.wait_ns, abort_flag));
+                    if (!ok) break;
+                    uint8_t *vt = smem + VF_OFF_V + (jj % VF_VSTAGES) * VF_TILE_BYTES;
+                    for (int c = nvalid + lane; c < VF_KT; c += 32) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            *reinterpret_cast<uint4 *>(vt + c * 128 + k * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4 *>(vt + VF_HALF_BYTES + c * 128 + k * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar_p_full + (jj & 1) * 8);
+            }
+            if (!ok) break;
+            // ---- epilogue of the item: merge the copies (log-sum-exp weights), normalise, store
+            ok = __all_sync(0xffffffffu, vf_wait(bar_o_full, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            float o[VF_D];
+            tmem_ld_cols<VF_D>(tmem + lane_base + VF_COL_O, o);
+            tc_fence_before();
+            mbar_arrive(bar_o_free);
+            mlx[warp * VF_ROWS + n] = make_float2(m_ref, l);
+            mbar_arrive(bar_ml);
+            ok = __all_sync(0xffffffffu, vf_wait(bar_ml, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+            if (!ok) break;
+            float mc[4], lc[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 v = mlx[c * VF_ROWS + n];
+                mc[c] = v.x;
+                lc[c] = v.y;
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < NSLICE; ++c) M = fmaxf(M, mc[c]);
+            const float Muse = M == -INFINITY ? 0.f : M;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < NSLICE; ++c) lsum += mc[c] == -INFINITY ? 0.f : ex2_approx(mc[c] - Muse) * lc[c];
+            const float wown = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - Muse);
+#pragma unroll
+            for (int c = 0; c < VF_D; ++c) o[c] *= wown;
+            // sum the four copies' rows: warps 2, 3 hand theirs to warps 0, 1; then warp 1 to warp 0
+            if (warp >= 2) {
+                float *dst = stage + ((warp - 2) * VF_ROWS + n) * VF_ST_STRIDE;
+#pragma unroll
+                for (int c = 0; c < VF_D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                mbar_arrive(bar_st1);
+            } else {
+                ok = __all_sync(0xffffffffu, vf_wait(bar_st1, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+                if (!ok) break;
+                const float *src = stage + (warp * VF_ROWS + n) * VF_ST_STRIDE;
+#pragma unroll
+                for (int c = 0; c < VF_D; c += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + c);
+                    o[c] += x.x;
+                    o[c + 1] += x.y;
+                    o[c + 2] += x.z;
+                    o[c + 3] += x.w;
+                }
+                if (warp == 1) {
+                    float *dst = stage + (VF_ROWS + n) * VF_ST_STRIDE;
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < VF_D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                    mbar_arrive(bar_st2);
+                } else {
+                    ok = __all_sync(0xffffffffu, vf_wait(bar_st2, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+                    if (!ok) break;
+                    const float *src1 = stage + (VF_ROWS + n) * VF_ST_STRIDE;
+#pragma unroll
+                    for (int c = 0; c < VF_D; c += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(src1 + c);
+                        o[c] += x.x;
+                        o[c + 1] += x.y;
+                        o[c + 2] += x.z;
+                        o[c + 3] += x.w;
+                    }
+                    if (n < p.rows) {
+                        const int64_t orow = ((int64_t)it.b * p.q_len + qi) * p.Hq + it.g * p.G + (n - qi * p.G);
+                        // a sequence that fits one partition is written directly (the merge skips it)
+                        if (p.part0 == 0 && it.L <= p.part_tokens) {
+                            const float inv = 1.f / lsum;
+                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + orow * VF_D);
+#pragma unroll
+                            for (int c = 0; c < VF_D; c += 8)
+                                dst[c / 8] = make_uint4(pack2<T>(o[c] * inv, o[c + 1] * inv), pack2<T>(o[c + 2] * inv, o[c + 3] * inv),
+                                                        pack2<T>(o[c + 4] * inv, o[c + 5] * inv), pack2<T>(o[c + 6] * inv, o[c + 7] * inv));
+                        } else {
+                            const int64_t prow = orow * p.max_parts + it.part;
+                            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * VF_D);
+#pragma unroll
+                            for (int c = 0; c < VF_D; c += 4) dst[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                            p.part_ml[prow] = make_float2(M, lsum);
+                        }
+                    }
+                }
+            }
+            ++ii;
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        // a wait ran out: record it, then wait (bounded) for every copy and MMA still in flight so that
+        // none lands in shared or tensor memory after the CTA has released them
+        if (tid == 0) set_status(p.status, STATUS_TIMEOUT);
+        if (warp == VF_MMA_WARP && lane == 0) {
+            int ik = 0, iv = 0;
+            for (int i = 0; i < 4; ++i) {
+                ik = max(ik, (int)issued[i]);
+                iv = max(iv, (int)issued[4 + i]);
+            }
+            for (int j = consumed_k; j < ik; ++j)
+                mbar_wait_bounded(bar_k_full + (j % VF_KSTAGES) * 8, (uint32_t)(j / VF_KSTAGES) & 1u, p.wait_ns);
+            for (int j = consumed_v; j < iv; ++j)
+                mbar_wait_bounded(bar_v_full + (j % VF_VSTAGES) * 8, (uint32_t)(j / VF_VSTAGES) & 1u, p.wait_ns);
+            umma_commit(bar_drain);
+            mbar_wait_bounded(bar_drain, 0u, p.wait_ns);
+        }
+        __syncthreads();
+    }
+    if (warp == VF_MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, VF_TMEM_COLS);
+    }
+}
+
+template <typename T>
+static cudaError_t launch_verify_t(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                   cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, VF_SMEM);
+    if (e != cudaSuccess) return e;
+    verify_kernel<T><<<(unsigned)grid, VF_THREADS, VF_SMEM, stream>>>(tmk, tmv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                          int max_ctas, cudaStream_t stream) {
+    if (p.rows < 1 || p.rows > VF_ROWS) return cudaErrorInvalidValue;
+    const int64_t items = (int64_t)p.num_seqs * p.Hkv * (p.max_parts - p.part0);
+    const int grid = (int)(items < max_ctas ? items : max_ctas);
+    if (grid < 1) return cudaSuccess;
+    return dtype == PA_FP16 ? launch_verify_t<__half>(p, tmk, tmv, grid, stream)
+                            : launch_verify_t<__nv_bfloat16>(p, tmk, tmv, grid, stream);
+}
+
+}  // namespace pa
