@@ -5,9 +5,11 @@ A step is one pass of the hot path over one batch: for every layer pool, the cac
 of the newest tokens (pa_cache_write) and the paged decode (pa_decode: decode kernel plus
 the partition merge). Default workload: Llama-3-70B-shaped decode, 64 sequences x 8192
 tokens, Hq 64 / Hkv 8 / d 128, block size 16, fp16, 80 independent layer pools (172 GB of
-KV, far larger than L2, so no flush is needed between steps).
+KV, far larger than L2, so no flush is needed between steps). The same run then times the
+long-context split decode (4 sequences x 131072 tokens, 512-token partitions) and reports it
+in the line's `secondary` object (`--no-secondary` skips it).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3|cfg5|cfg2|cfg4|cfg1]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3|cfg5|cfg2|cfg4|cfg1|verify70b]
     python bench.py --impl reference      # the fp64 CPU oracle as the reference arm
     python bench.py --workload prefill    # chunked prefill (pa_prefill), tensor-core bound: TFLOP/s
     python bench.py --workload cow        # copy-on-write block copies (pa_copy_blocks): GB/s
@@ -35,13 +37,16 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 import synth  # noqa: E402
 
-WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "prefill": 0, "cow": -1, "spec": -2}
+WORKLOADS = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "verify70b": 6, "prefill": 0, "cow": -1,
+             "spec": -2}
 DESCR = {
     1: "tiny paged decode (B4, lens 17/64/100/200, Hq8 Hkv2 d64 bs16, fp16)",
     2: "Llama-3-8B-shaped decode layer (B64, lens U[512,4096], Hq32 Hkv8 d128 bs16, bf16)",
     3: "Llama-3-70B-shaped decode, 80 layer pools (B64, ctx 8192, Hq64 Hkv8 d128 bs16, fp16)",
     4: "shared 1024-token prefix + 5-token causal verify (B128, suffix U[64,512], Hq32 Hkv8 d128 bs16, bf16)",
     5: "long-context split decode (B4, ctx 131072, Hq32 Hkv8 d128 bs32, fp16, 512-token partitions)",
+    6: "Llama-3-70B-shaped speculative verify: 64 sequences x 8192 tokens, 4 draft tokens each (q_len 4; Hq64 Hkv8: "
+       "32 query rows per KV head, the tensor-core decode kernel), d128 bs16, fp16, one layer pool",
     0: "chunked prefill, Llama-3-70B-shaped: 8 sequences each attending with a 512-token chunk that ends at "
        "context 4608 (the 9th chunk of the prompt), Hq64 Hkv8 d128 bs16, 8 layer pools",
 }
@@ -52,6 +57,13 @@ DESCR[-2] = ("speculative rejection sampling: 128 sequences x 5 drafts over a 12
              "target and draft distributions, seeded)")
 COW = dict(num_blocks=32768, Hkv=8, bs=16, d=128, pairs=4096)
 SPEC = dict(B=128, K=5, V=128256)
+
+
+def make_workload(k: int, layers=None, batch=None) -> synth.Workload:
+    """The decode workloads: the five of synth.workload, and the 70B-shaped 4-draft verify (k = 6)."""
+    if k == 6:
+        return synth.custom_workload([8192] * (batch or 64), 64, 8, 128, 16, 4, synth.FP16, tag=600)
+    return synth.workload(k, layers=layers, batch=batch)
 
 
 def dist_env():
@@ -74,6 +86,7 @@ def peaks():
 # launch shape (partitions per CTA, row tiles), the entry points
 TRAFFIC_SOURCES = {
     "decode": ("decode.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"),
+    "verify": ("verify.cu", "decode.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"),
     "spec": ("spec_verify.cu", "pa_device.cuh", "pa_internal.h"),
     "cow": ("copy_blocks.cu", "pa_device.cuh", "pa_internal.h"),
     "prefill": ("prefill.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"),
@@ -236,32 +249,16 @@ def step_bytes(wl: synth.Workload, kv_format: int = 0):
     return wl.layers * (dec + cw), dec
 
 
-def run_gpu(args):
+def time_decode_steps(G: "GpuWorkload", steps: int, warmup: int, dev, barrier):
+    """Warm-up, then `steps` timed steps with CUDA events around the whole region and around each decode call.
+    Returns (elapsed ms of the region on this rank, per-call ms list, clock summary)."""
     import torch
-    import torch.distributed as dist
-    ws, rank, local = dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    k = WORKLOADS[args.workload]
-    wl = synth.workload(k, layers=args.layers, batch=args.batch)
-    kv_format = 1 if args.kv == "fp8" else 0
-    G = GpuWorkload(wl, dev, kv_format, args.shared_prefix)
-    total_bytes, decode_bytes = step_bytes(wl, kv_format)
-    kv_tokens = int(wl.context_lens.sum()) * wl.layers
-
-    def barrier():
-        torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         G.step()
     barrier()
     nl = len(G.layers)
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -272,23 +269,80 @@ def run_gpu(args):
         time.sleep(0.3)
         barrier()
         start.record()
-        for s in range(args.steps):
+        for s in range(steps):
             G.step(evs[s])
         stop.record()
         barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    dec_ms = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps) for i in range(nl)]
+    dec_ms = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps) for i in range(nl)]
+    return start.elapsed_time(stop), dec_ms, clk.summary()
+
+
+def decode_roofline(decode_bytes: int, dec_ms, traffic, kernel: str):
+    """Roofline of the decode call: algorithmic bytes over the mean call time (CUDA events on the launching
+    stream), against the measured HBM copy rate; median and minimum call times beside the mean."""
+    peak, peak_kind = peaks()
+    avg = float(np.mean(dec_ms))
+    achieved = decode_bytes / (avg * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+            "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(avg, 5),
+            "median_launch_ms": round(float(np.median(dec_ms)), 5), "min_launch_ms": round(float(np.min(dec_ms)), 5),
+            "frac_at_median": round(decode_bytes / (float(np.median(dec_ms)) * 1e-3) / 1e9 / peak, 4),
+            "peak_kind": peak_kind}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    k = WORKLOADS[args.workload]
+    wl = make_workload(k, layers=args.layers, batch=args.batch)
+    kv_format = 1 if args.kv == "fp8" else 0
+    G = GpuWorkload(wl, dev, kv_format, args.shared_prefix)
+    total_bytes, decode_bytes = step_bytes(wl, kv_format)
+    kv_tokens = int(wl.context_lens.sum()) * wl.layers
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+
+    elapsed_ms, dec_ms, clocks = time_decode_steps(G, args.steps, args.warmup, dev, barrier)
     elapsed_ms = reduce_max(elapsed_ms, dev)
     ms_per_step = elapsed_ms / args.steps
     value = job_value(total_bytes, args.steps, elapsed_ms, ws)
 
     # end to end through the public API: pinned host inputs -> device, kernels, result -> host
     e2e = None if args.no_e2e else run_e2e(G, wl, dev, max(3, args.steps // 5), barrier, kv_format)
+    launches = G.launches_per_step() * args.steps
+    assert G.pool.check() == 0, "device status flagged during the decode benchmark"
+
+    # the long-context workload (graded beside the 70B-shaped one) in the same run, as a secondary object
+    secondary = None
+    if args.workload == "cfg3" and not kv_format and not args.no_secondary:
+        del G
+        torch.cuda.empty_cache()
+        wl5 = synth.workload(5)
+        G5 = GpuWorkload(wl5, dev, 0, False)
+        tb5, db5 = step_bytes(wl5, 0)
+        el5, dm5, clk5 = time_decode_steps(G5, args.steps, args.warmup, dev, barrier)
+        el5 = reduce_max(el5, dev)
+        assert G5.pool.check() == 0, "device status flagged during the long-context benchmark"
+        secondary = {
+            "workload": f"cfg5: {DESCR[5]}", "config": synth.describe(wl5),
+            "value": round(job_value(tb5, args.steps, el5, ws), 2), "unit": "GB/s", "steps": args.steps,
+            "ms_per_step": round(el5 / args.steps, 4),
+            "kv_tokens_per_s": round(ws * int(wl5.context_lens.sum()) * args.steps / (el5 * 1e-3), 1),
+            "roofline": decode_roofline(db5, dm5, measured_traffic("cfg5"),
+                                        "pa_decode call (decode kernel + partition merge)"),
+            "gpu_launches": G5.launches_per_step() * args.steps, "clocks": clk5,
+            "l2": "inputs larger than L2 (no flush)"}
 
     if rank == 0:
-        peak, peak_kind = peaks()
-        dec_avg_ms = float(np.mean(dec_ms))
-        achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
         line = {
             "metric": "paged-attn decode KV GB/s & KV tokens/s on 1 GB300 (fraction of HBM peak)",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -296,22 +350,22 @@ def run_gpu(args):
             "dtype": ("fp16" if wl.dtype == synth.FP16 else "bf16") + ("+fp8-kv" if kv_format else ""),
             "data": "synthetic (seeded, N(0,1)-shaped)",
             "config": {**synth.describe(wl), "workload": f"{args.workload}: {DESCR[k]}",
-                       "decode_call": "pa_decode_shared_prefix" if G.shared_prefix else "pa_decode",
+                       "decode_call": "pa_decode_shared_prefix" if args.shared_prefix and wl.prefix_tokens else "pa_decode",
                        "kv_cache": "fp8 e4m3 + fp32 scale per (slot, head)" if kv_format else "16-bit",
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{ws}"},
             "kv_tokens_per_s": round(ws * kv_tokens * args.steps / (elapsed_ms * 1e-3), 1),
-            "fraction_of_hbm_peak": round(value / peak, 4),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4),
-                         "traffic": None if kv_format else measured_traffic(args.workload),
-                         "kernel": ("pa_decode_shared_prefix call (prefix kernel + suffix decode + merge)"
-                                    if G.shared_prefix else "pa_decode call (decode kernel + partition merge)"),
-                         "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
-                         "peak_kind": peak_kind},
+            "fraction_of_hbm_peak": round(value / peaks()[0], 4),
+            "roofline": decode_roofline(
+                decode_bytes, dec_ms,
+                None if kv_format else measured_traffic(args.workload, "verify" if k == 6 else "decode"),
+                "pa_decode_shared_prefix call (prefix kernel + suffix decode + merge)"
+                if args.shared_prefix and wl.prefix_tokens else "pa_decode call (decode kernel + partition merge)"),
             "e2e": e2e,
-            "gpu_launches": G.launches_per_step() * args.steps,
-            "clocks": clk.summary(),
+            "gpu_launches": launches,
+            "clocks": clocks,
         }
+        if secondary:
+            line["secondary"] = secondary
         if ws == 1 and not args.no_cpu_baseline and not kv_format:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -841,7 +895,7 @@ def run_reference(args):
     if k < 0:
         run_aux_reference(args, k)
         return
-    wl = synth.workload(k, layers=1)
+    wl = make_workload(k, layers=1)
     nseq = pick_nseq(wl, args.ref_step_seconds)
     hk, hv, news, q = oracle_sample(wl, nseq)
     for _ in range(args.warmup):
@@ -853,7 +907,7 @@ def run_reference(args):
     dt = (time.perf_counter() - t0) / args.steps
     nbytes, toks = sample_bytes(wl, nseq)
     value = round(nbytes / dt / 1e9, 4)
-    wl_full = synth.workload(k, layers=1 if k != 3 else 80)
+    wl_full = make_workload(k, layers=1 if k != 3 else 80)
     line = {"impl": "reference",
             "metric": "paged-attn decode KV GB/s & KV tokens/s on 1 GB300 (fraction of HBM peak)",
             "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -942,6 +996,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="layer pools (cfg3: default 80; prefill: default 8)")
     ap.add_argument("--batch", type=int, default=None, help="sequences (default: the workload's)")
     ap.add_argument("--dtype", default="fp16", choices=sorted(synth.DTYPES), help="prefill workload dtype")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload: skip the long-context workload timed after it in the same run")
     ap.add_argument("--shared-prefix", action="store_true",
                     help="decode workloads with a shared prefix (cfg4) through pa_decode_shared_prefix")
     args = ap.parse_args()
