@@ -394,13 +394,10 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
             }
         }
     }
-    // a persistent suffix decode (the tensor-core kernel, for more than 8 rows per KV head) takes the SMs
-    // the prefix kernel leaves free, so that the two run side by side
-    {
-        const int64_t ctiles = (((int64_t)num_seqs * p.rows + 127) / 128 + 1) / 2;
-        const int64_t prefix_ctas = ctiles * p.Hkv * ((p.part0 + p.pchunk - 1) / p.pchunk);
-        p.vf_ctas = prefix_ctas < pool->sm_count ? (int)(pool->sm_count - prefix_ctas) : pool->sm_count;
-    }
+    // the suffix decode keeps the many-CTA kernel of decode.cu: its items are short (the prefix is done by the
+    // prefix kernel), and the persistent tensor-core kernel's per-item epilogue outweighs its gain there
+    // (shared-prefix verify workload: 0.127 vs 0.076 ms per call)
+    p.allow_verify = false;
     // the prefix kernel (tensor cores, one CTA per SM) goes first, straight onto the caller's stream, so
     // that its CTAs take whole SMs before the suffix decode (bandwidth, many small CTAs, on the pool's
     // side stream) fills the rest; the merge waits for both

@@ -26,8 +26,12 @@
 //
 // One persistent CTA per SM walks its items (c, c + grid, ...); every role follows the same
 // sequence of tiles, so the copies of the next item start while the current one finishes.
-//   warps 0-3   softmax of copy w (quarter w), then the epilogue: copies merged through shared memory,
-//               rows normalised and stored.
+//   warps 0-3   softmax of copy w (quarter w), then the epilogue: each copy's rows, scaled to the common
+//               max, go to shared memory; warp w sums the four copies of rows 8w..8w+7 and stores them
+//               (coalesced). Every sub-partition also hosts an issuing warp, and a
+//               warp scheduler that keeps picking a busy softmax warp starves it (an MMA issued from a
+//               sub-partition shared with one busy FP32 warp took 235 instead of 65 cycles), so the
+//               softmax yields its issue slot (nanosleep 0) every 16 exponentials.
 //   warp 4      MMA issue (one thread) and tensor-memory allocation.
 //   warps 8-11  K producers, warps 12-15 V producers: each warp copies two 16-key sub-tiles of every
 //               tile, one TMA box per 64-dimension half; block ids looked up one tile ahead (one warp's
@@ -42,18 +46,18 @@ namespace pa {
 constexpr int VF_KT = 128;                             // keys per tile
 constexpr int VF_D = 128;                              // head dimension
 constexpr int VF_ROWS = 32;                            // query rows per KV head, at most
-constexpr int VF_KSTAGES = 3, VF_VSTAGES = 2;
+constexpr int VF_KSTAGES = 2, VF_VSTAGES = 2;
 constexpr int VF_TILE_BYTES = VF_KT * VF_D * 2;        // 32 KB: K or V tile, [2 halves][128 keys][128 B]
 constexpr int VF_HALF_BYTES = VF_KT * 128;             // 16 KB
 constexpr int VF_ST_STRIDE = VF_D + 4;                 // fp32 staging row (padded: no bank conflicts)
 constexpr int VF_OFF_K = 0;
 constexpr int VF_OFF_V = VF_OFF_K + VF_KSTAGES * VF_TILE_BYTES;
-constexpr int VF_OFF_ST = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;   // staging [2][32 rows][VF_ST_STRIDE] fp32
-constexpr int VF_OFF_ML = VF_OFF_ST + 2 * VF_ROWS * VF_ST_STRIDE * 4;  // (max, sum) per copy and row [4][32]
-constexpr int VF_OFF_BAR = VF_OFF_ML + 4 * VF_ROWS * 8;
-// barriers: k_full[3] k_empty[3] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
-//           o_full o_free ml st1 st2 drain
-constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6;
+constexpr int VF_OFF_ST = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;   // staging [4 copies][32 rows][VF_ST_STRIDE] fp32
+constexpr int VF_OFF_ML = VF_OFF_ST + 4 * VF_ROWS * VF_ST_STRIDE * 4;  // (max, sum) per copy and row [4][32], merged [32]
+constexpr int VF_OFF_BAR = VF_OFF_ML + 5 * VF_ROWS * 8;
+// barriers: k_full[2] k_empty[2] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
+//           o_full o_free ml st drain
+constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 5;
 constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4]
 constexpr int VF_SMEM = 1024 + VF_OFF_MISC + 64;
 static_assert(VF_OFF_BAR % 8 == 0, "barrier alignment");
@@ -81,22 +85,34 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     return pol;
 }
 
-// Bounded wait that also gives up when another role has aborted the CTA. Roles that run ahead of the
-// others (copies, Q loads) pass a back-off: between polls they sleep instead of taking issue slots from
-// the softmax warps that share their sub-partitions.
+// One poll of a barrier phase that suspends the thread (up to `hint_ns`) until the phase completes
+// instead of returning at once: waiting threads give their sub-partition's issue slots to the others.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait that also gives up when another role has aborted the CTA. Each poll suspends for up
+// to 1 us (the phase's completion ends it early); roles that run ahead of the others (copies, Q loads)
+// pass a back-off and also sleep between polls.
 __device__ __forceinline__ bool vf_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort_flag,
                                         uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (sleep_ns) __nanosleep(sleep_ns);
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 || sleep_ns) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > limit_ns) {
-                *abort_flag = 1;
-                return false;
-            }
+        if (mbar_try_wait_suspend(bar, parity, 1000u)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -167,13 +183,13 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     const uint32_t bar_o_free = bar_o_full + 8;
     const uint32_t bar_ml = bar_o_free + 8;
     const uint32_t bar_st1 = bar_ml + 8;
-    const uint32_t bar_st2 = bar_st1 + 8;
-    const uint32_t bar_drain = bar_st2 + 8;
+    const uint32_t bar_drain = bar_st1 + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + VF_OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *issued = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [K warps 0..3, V warps 0..3]
-    float *stage = reinterpret_cast<float *>(smem + VF_OFF_ST);                // [2][32][VF_ST_STRIDE]
+    float *stage = reinterpret_cast<float *>(smem + VF_OFF_ST);                // [4][32][VF_ST_STRIDE]
     float2 *mlx = reinterpret_cast<float2 *>(smem + VF_OFF_ML);                // [4 copies][32 rows]
+    float2 *mlm = mlx + 4 * VF_ROWS;                                           // merged (max, sum) [32 rows]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nlaunch = p.max_parts - p.part0;
@@ -200,8 +216,7 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         mbar_init(bar_o_full, 1);
         mbar_init(bar_o_free, 128);
         mbar_init(bar_ml, 128);
-        mbar_init(bar_st1, 64);
-        mbar_init(bar_st2, 32);
+        mbar_init(bar_st1, 128);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         for (int i = 0; i < 8; ++i) issued[i] = 0;
@@ -352,6 +367,12 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                         break;
                     const uint32_t qcol = tmem + VF_COL_Q + (ii & 1) * 64;
                     for (int t = 0; t < it.ntiles; ++t, ++jj) {
+                        // the previous item's last P.V first: its epilogue waits on it, the first S of this item
+                        // is not needed before that epilogue ends
+                        if (t == 0 && pv_jj >= 0) {
+                            if (!(ok = do_pv())) break;
+                            pv_jj = -1;
+                        }
                         if (!(ok = vf_wait(bar_k_full + (jj % VF_KSTAGES) * 8, (uint32_t)(jj / VF_KSTAGES) & 1u,
                                            p.wait_ns, abort_flag)))
                             break;
@@ -425,6 +446,7 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                     }
                 }
                 const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+                __nanosleep(0);   // let the MMA warp of this sub-partition issue
                 float alpha = 1.f;
                 bool rescale = false;
                 if (mx > m_ref + VF_RESCALE_LOG2 || (m_ref == -INFINITY && mx > -INFINITY)) {
@@ -455,6 +477,7 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                 for (int c = 0; c < SW; ++c) {
                     sv[c] = ex2_approx(fmaf(sv[c], p.scale_log2, nmuse));
                     r4[c & 3] += sv[c];
+                    if ((c & 15) == 15) __nanosleep(0);
                 }
                 l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
                 // P4 row: 128 keys as 64 packed columns; this copy's slice holds its weights (the high or the low
@@ -523,76 +546,55 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
             mbar_arrive(bar_ml);
             ok = __all_sync(0xffffffffu, vf_wait(bar_ml, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
             if (!ok) break;
-            float mc[4], lc[4];
+            {
+                float M = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float2 v = mlx[c * VF_ROWS + n];
-                mc[c] = v.x;
-                lc[c] = v.y;
-            }
-            float M = -INFINITY;
+                for (int c = 0; c < NSLICE; ++c) M = fmaxf(M, mlx[c * VF_ROWS + n].x);
+                const float Muse = M == -INFINITY ? 0.f : M;
+                float lsum = 0.f;
 #pragma unroll
-            for (int c = 0; c < NSLICE; ++c) M = fmaxf(M, mc[c]);
-            const float Muse = M == -INFINITY ? 0.f : M;
-            float lsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < NSLICE; ++c) lsum += mc[c] == -INFINITY ? 0.f : ex2_approx(mc[c] - Muse) * lc[c];
-            const float wown = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - Muse);
-#pragma unroll
-            for (int c = 0; c < VF_D; ++c) o[c] *= wown;
-            // sum the four copies' rows: warps 2, 3 hand theirs to warps 0, 1; then warp 1 to warp 0
-            if (warp >= 2) {
-                float *dst = stage + ((warp - 2) * VF_ROWS + n) * VF_ST_STRIDE;
-#pragma unroll
-                for (int c = 0; c < VF_D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-                mbar_arrive(bar_st1);
-            } else {
-                ok = __all_sync(0xffffffffu, vf_wait(bar_st1, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
-                if (!ok) break;
-                const float *src = stage + (warp * VF_ROWS + n) * VF_ST_STRIDE;
-#pragma unroll
-                for (int c = 0; c < VF_D; c += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(src + c);
-                    o[c] += x.x;
-                    o[c + 1] += x.y;
-                    o[c + 2] += x.z;
-                    o[c + 3] += x.w;
+                for (int c = 0; c < NSLICE; ++c) {
+                    const float2 v = mlx[c * VF_ROWS + n];
+                    lsum += v.x == -INFINITY ? 0.f : ex2_approx(v.x - Muse) * v.y;
                 }
-                if (warp == 1) {
-                    float *dst = stage + (VF_ROWS + n) * VF_ST_STRIDE;
-                    __syncwarp();
+                if (warp == 0) mlm[n] = make_float2(M, lsum);
+                // this copy's rows, scaled to the common max, into its staging rows
+                const float wown = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - Muse);
+                float *dst = stage + (warp * VF_ROWS + n) * VF_ST_STRIDE;
 #pragma unroll
-                    for (int c = 0; c < VF_D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-                    mbar_arrive(bar_st2);
-                } else {
-                    ok = __all_sync(0xffffffffu, vf_wait(bar_st2, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
-                    if (!ok) break;
-                    const float *src1 = stage + (VF_ROWS + n) * VF_ST_STRIDE;
+                for (int c = 0; c < VF_D; c += 4)
+                    *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c] * wown, o[c + 1] * wown, o[c + 2] * wown,
+                                                                       o[c + 3] * wown);
+            }
+            mbar_arrive(bar_st1);
+            ok = __all_sync(0xffffffffu, vf_wait(bar_st1, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+            if (!ok) break;
+            // warp w sums the copies of rows 8w..8w+7 and stores them, one row per step, 4 dims per lane (every
+            // row is read and written as one contiguous run)
+            {
+                const bool direct = p.part0 == 0 && it.L <= p.part_tokens;   // the merge skips such sequences
+#pragma unroll 1
+                for (int r = warp * 8; r < warp * 8 + 8 && r < p.rows; ++r) {
+                    float4 acc = *reinterpret_cast<const float4 *>(stage + r * VF_ST_STRIDE + 4 * lane);
 #pragma unroll
-                    for (int c = 0; c < VF_D; c += 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(src1 + c);
-                        o[c] += x.x;
-                        o[c + 1] += x.y;
-                        o[c + 2] += x.z;
-                        o[c + 3] += x.w;
+                    for (int c = 1; c < 4; ++c) {
+                        const float4 x = *reinterpret_cast<const float4 *>(stage + (c * VF_ROWS + r) * VF_ST_STRIDE + 4 * lane);
+                        acc.x += x.x;
+                        acc.y += x.y;
+                        acc.z += x.z;
+                        acc.w += x.w;
                     }
-                    if (n < p.rows) {
-                        const int64_t orow = ((int64_t)it.b * p.q_len + qi) * p.Hq + it.g * p.G + (n - qi * p.G);
-                        // a sequence that fits one partition is written directly (the merge skips it)
-                        if (p.part0 == 0 && it.L <= p.part_tokens) {
-                            const float inv = 1.f / lsum;
-                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + orow * VF_D);
-#pragma unroll
-                            for (int c = 0; c < VF_D; c += 8)
-                                dst[c / 8] = make_uint4(pack2<T>(o[c] * inv, o[c + 1] * inv), pack2<T>(o[c + 2] * inv, o[c + 3] * inv),
-                                                        pack2<T>(o[c + 4] * inv, o[c + 5] * inv), pack2<T>(o[c + 6] * inv, o[c + 7] * inv));
-                        } else {
-                            const int64_t prow = orow * p.max_parts + it.part;
-                            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * VF_D);
-#pragma unroll
-                            for (int c = 0; c < VF_D; c += 4) dst[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-                            p.part_ml[prow] = make_float2(M, lsum);
-                        }
+                    const float2 ml = mlm[r];
+                    const int rqi = r / p.G;
+                    const int64_t orow = ((int64_t)it.b * p.q_len + rqi) * p.Hq + it.g * p.G + (r - rqi * p.G);
+                    if (direct) {
+                        const float inv = 1.f / ml.y;
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<T *>(p.out) + orow * VF_D + 4 * lane) =
+                            make_uint2(pack2<T>(acc.x * inv, acc.y * inv), pack2<T>(acc.z * inv, acc.w * inv));
+                    } else {
+                        const int64_t prow = orow * p.max_parts + it.part;
+                        *reinterpret_cast<float4 *>(p.part_o + prow * VF_D + 4 * lane) = acc;
+                        if (lane == 0) p.part_ml[prow] = ml;
                     }
                 }
             }

@@ -1,6 +1,6 @@
-"""The tensor-core decode kernel (25..32 query rows per KV head) against the fp64 oracle.
+"""The tensor-core decode kernel (9..32 query rows per KV head) against the fp64 oracle.
 
-pa_decode routes a KV head's query rows to this kernel when there are more than 24 of them (a wide
+pa_decode routes a KV head's query rows to this kernel when there are more than 8 of them (a wide
 GQA group, or draft rows of a verify pass: q_len * G), for 16-bit pools with head_dim 128. These
 cases cover its item walk (several items per CTA, partitions merged or written directly), the
 keys past an item (context end and partition ends that are not multiples of its 128-key tile),
@@ -27,13 +27,16 @@ CASES = [
     ([9, 100, 2049], 32, 8, 16, 8, synth.BF16, 0, 512),            # q_len 8, G = 4
     ([1024 + 40, 1024 + 300, 1024 + 511], 32, 4, 16, 4, synth.BF16, 1024, 512),   # shared copy-on-write prefix
     ([32768, 20000], 64, 2, 32, 1, synth.FP16, 0, 512),            # one 32-head group, long contexts
+    ([80, 600, 4], 24, 8, 16, 4, synth.FP16, 0, 512),              # 12 rows (G = 3, q_len 4), context = q_len
+    ([5000, 17], 16, 1, 32, 1, synth.BF16, 0, 256),                # 16 rows: one 16-head group
+    ([1300, 1100, 1536], 32, 8, 16, 5, synth.BF16, 0, 512),        # 20 rows: the verify workload's shape
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"tc{i}" for i in range(len(CASES))])
 def test_tensor_core_decode_matches_oracle(case):
     lens, Hq, Hkv, bs, ql, dt, pre, part = case
-    assert 24 < Hq // Hkv * ql <= 32
+    assert 8 < Hq // Hkv * ql <= 32
     wl = synth.custom_workload(lens, Hq, Hkv, 128, bs, ql, dt, prefix_tokens=pre, partition_tokens=part,
                                tag=400 + CASES.index(case))
     pool, kc, vc, q, tables, lens_d = H.build_device(wl)
