@@ -9,29 +9,28 @@
 // the decode's (sequence, KV head, context partition) triples, so partial states and the
 // log-sum-exp merge are shared with decode.cu.
 //
-// Per 128-key tile, with the query rows on the M side (row r of a copy in tensor-memory lane r of
-// that copy's quarter):
-//   S [128 x 128 keys] = Q4 [128 x 128 d] . K_tile^T   (M128 N128 K16 x 8; Q4 in tensor memory)
-//   O [128 x 128 d]   += P4 [128 x 128 keys] . V_tile   (M128 N128 K16 x 8; P4 in tensor memory)
-// Q4 holds four copies of the head group's (up to 32) query rows, one per 32-lane quarter, so that
-// all four sub-partitions of the SM take part in the softmax (a warp reaches only its own quarter,
-// and an exponential costs the same per warp instruction however many lanes are active). Each copy
-// owns a slice of every tile's keys and runs its own online softmax over that slice (its own running
-// max and sum); its weights outside the slice are zero, so its O rows accumulate only its slice. The
-// epilogue merges the copies with the log-sum-exp rule. fp16: four slices of 32 keys. bf16: two
-// slices of 64 keys, each held by two copies, one writing the weights' high parts (bf16(p)) and one
-// the low parts (bf16(p - hi)), so that P keeps 16 significant bits (8 alone fail the tolerance
-// where weighted values cancel) with no extra tensor-core work. K and V tiles are read from shared
-// memory once per tile each; Q and P never touch it.
+// Per 128-key tile:
+//   S   [128 x 128 keys] = Q4 [128 x 128 d] . K_tile^T     (M128 N128 K16 x 8; Q4 in tensor memory)
+//   O^T [128 d x NP]    += V_tile^T [128 d x 128 keys] . P^T [128 keys x NP]   (M128 N{64,32} K16 x 8)
+// Q4 holds four copies of the head group's (up to 32) query rows, one per 32-lane quarter of tensor
+// memory, so that each of the four softmax warps (a warp reaches only its own quarter) reads every
+// row's scores for its own slice of 32 keys of the tile. The four slices share one running maximum
+// per row (exchanged through shared memory each tile), so their weights are on one scale: each warp
+// writes its slice of P^T (query rows on the N side) into shared memory and one product per tile
+// accumulates every slice into O^T (head dimension on the lanes, one column per query row). bf16
+// weights are carried as high parts bf16(p) in columns 0..31 and low parts bf16(p - hi) in columns
+// 32..63 (8 significant bits alone fail the tolerance where weighted values cancel; the two halves
+// cost one N = 64 product); fp16 needs only the 32 columns. The epilogue of an item is a read of
+// O^T (each thread one dimension of every row) and coalesced row stores: no merge between warps.
+// K and V tiles are read from shared memory by the tensor cores once per tile each.
 //
 // One persistent CTA per SM walks its items (c, c + grid, ...); every role follows the same
 // sequence of tiles, so the copies of the next item start while the current one finishes.
-//   warps 0-3   softmax of copy w (quarter w), then the epilogue: each copy's rows, scaled to the common
-//               max, go to shared memory; warp w sums the four copies of rows 8w..8w+7 and stores them
-//               (coalesced). Every sub-partition also hosts an issuing warp, and a
-//               warp scheduler that keeps picking a busy softmax warp starves it (an MMA issued from a
-//               sub-partition shared with one busy FP32 warp took 235 instead of 65 cycles), so the
-//               softmax yields its issue slot (nanosleep 0) every 16 exponentials.
+//   warps 0-3   softmax of key slice w (rows of quarter w), then the item's epilogue: warp w stores
+//               dimensions 32w..32w+31 of every row. Every sub-partition also hosts an issuing warp,
+//               and a warp scheduler that keeps picking a busy softmax warp starves it (an MMA issued
+//               from a sub-partition shared with one busy FP32 warp took 235 instead of 65 cycles),
+//               so the softmax yields its issue slot (nanosleep 0) every 16 exponentials.
 //   warp 4      MMA issue (one thread) and tensor-memory allocation.
 //   warps 8-11  K producers, warps 12-15 V producers: each warp copies two 16-key sub-tiles of every
 //               tile, one TMA box per 64-dimension half; block ids looked up one tile ahead (one warp's
@@ -49,15 +48,17 @@ constexpr int VF_ROWS = 32;                            // query rows per KV head
 constexpr int VF_KSTAGES = 2, VF_VSTAGES = 2;
 constexpr int VF_TILE_BYTES = VF_KT * VF_D * 2;        // 32 KB: K or V tile, [2 halves][128 keys][128 B]
 constexpr int VF_HALF_BYTES = VF_KT * 128;             // 16 KB
-constexpr int VF_ST_STRIDE = VF_D + 4;                 // fp32 staging row (padded: no bank conflicts)
+constexpr int VF_SW = 32;                              // keys per slice: one slice per softmax warp
+constexpr int VF_P_BYTES = 16 * 1024;                  // one P^T buffer: [2 blocks of 64 keys][<= 64 rows][128 B]
 constexpr int VF_OFF_K = 0;
 constexpr int VF_OFF_V = VF_OFF_K + VF_KSTAGES * VF_TILE_BYTES;
-constexpr int VF_OFF_ST = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;   // staging [4 copies][32 rows][VF_ST_STRIDE] fp32
-constexpr int VF_OFF_ML = VF_OFF_ST + 4 * VF_ROWS * VF_ST_STRIDE * 4;  // (max, sum) per copy and row [4][32], merged [32]
-constexpr int VF_OFF_BAR = VF_OFF_ML + 5 * VF_ROWS * 8;
+constexpr int VF_OFF_P = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;    // P^T [2 buffers]
+constexpr int VF_OFF_O = VF_OFF_P + 2 * VF_P_BYTES;    // output rows of an item [32 rows][128 d] (fp32 or T)
+constexpr int VF_OFF_X = VF_OFF_O + VF_ROWS * VF_D * 4;   // slice maxima [2 tiles][32 rows][4], slice sums [32][4]
+constexpr int VF_OFF_BAR = VF_OFF_X + 3 * VF_ROWS * 4 * 4;
 // barriers: k_full[2] k_empty[2] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
-//           o_full o_free ml st drain
-constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 5;
+//           o_full o_free mx lx ost drain
+constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6;
 constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4]
 constexpr int VF_SMEM = 1024 + VF_OFF_MISC + 64;
 static_assert(VF_OFF_BAR % 8 == 0, "barrier alignment");
@@ -70,12 +71,23 @@ constexpr int VF_THREADS = 512;
 constexpr int VF_MMA_WARP = 4, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
 constexpr uint32_t VF_REGS_HIGH = 232, VF_REGS_LOW = 88;
 static_assert(128 * VF_REGS_HIGH + 384 * VF_REGS_LOW <= VF_THREADS * 128, "register split");
-// tensor memory: Q4[2] at columns 0 / 64 (128 d as 64 packed columns), S/P[2] at 128 / 256, O at 384
+// tensor memory: Q4[2] at columns 0 / 64 (128 d as 64 packed columns), S[2] at 128 / 256, O^T at 384 (64 columns)
 constexpr uint32_t VF_TMEM_COLS = 512;
 constexpr uint32_t VF_COL_Q = 0, VF_COL_S = 128, VF_COL_O = 384;
 constexpr float VF_RESCALE_LOG2 = 8.f;                 // stale-max headroom (P <= 2^8)
 
 size_t verify_smem_bytes() { return VF_SMEM; }
+
+template <typename T>
+__device__ __forceinline__ T vf_round(float x);
+template <>
+__device__ __forceinline__ __half vf_round<__half>(float x) {
+    return __float2half_rn(x);
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 vf_round<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
 
 // Copies keep the normal L2 priority: blocks shared by several tables (a copy-on-write prefix) are read
 // again by other CTAs, other blocks once.
@@ -164,8 +176,8 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
     constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int NSLICE = SPLIT_P ? 2 : 4;              // key slices per tile
-    constexpr int SW = VF_KT / NSLICE;                    // keys per slice (32 or 64)
+    constexpr int NP = SPLIT_P ? 64 : 32;                // P^T rows = O^T columns (bf16: high parts, then low parts)
+    constexpr int PBLK = NP * 128;                        // bytes of one 64-key block of P^T
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -181,15 +193,15 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     const uint32_t bar_pv_done = bar_p_full + 16;
     const uint32_t bar_o_full = bar_pv_done + 16;
     const uint32_t bar_o_free = bar_o_full + 8;
-    const uint32_t bar_ml = bar_o_free + 8;
-    const uint32_t bar_st1 = bar_ml + 8;
-    const uint32_t bar_drain = bar_st1 + 8;
+    const uint32_t bar_mx = bar_o_free + 8;
+    const uint32_t bar_lx = bar_mx + 8;
+    const uint32_t bar_ost = bar_lx + 8;
+    const uint32_t bar_drain = bar_ost + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + VF_OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *issued = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [K warps 0..3, V warps 0..3]
-    float *stage = reinterpret_cast<float *>(smem + VF_OFF_ST);                // [4][32][VF_ST_STRIDE]
-    float2 *mlx = reinterpret_cast<float2 *>(smem + VF_OFF_ML);                // [4 copies][32 rows]
-    float2 *mlm = mlx + 4 * VF_ROWS;                                           // merged (max, sum) [32 rows]
+    float *mxs = reinterpret_cast<float *>(smem + VF_OFF_X);                   // [2 tiles][32 rows][4 slices]
+    float *lsx = mxs + 2 * VF_ROWS * 4;                                        // [32 rows][4 slices]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nlaunch = p.max_parts - p.part0;
@@ -215,8 +227,9 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         }
         mbar_init(bar_o_full, 1);
         mbar_init(bar_o_free, 128);
-        mbar_init(bar_ml, 128);
-        mbar_init(bar_st1, 128);
+        mbar_init(bar_mx, 128);
+        mbar_init(bar_lx, 128);
+        mbar_init(bar_ost, 128);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         for (int i = 0; i < 8; ++i) issued[i] = 0;
@@ -329,14 +342,16 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
             // ------------------------------------------------------------------ MMA issue (lane 0)
             if (lane == 0) {
                 const uint32_t idesc_s = umma_idesc<T>(128, VF_KT, false);
-                const uint32_t idesc_o = umma_idesc<T>(128, VF_D, true);
+                // O^T = V^T P^T: A = the V tile read M(= d)-major (bit 15), B = P^T, K-major
+                const uint32_t idesc_o = umma_idesc<T>(128, NP, false) | (1u << 15);
                 const uint64_t dk0 = umma_desc_sw128(base + VF_OFF_K, 16, 1024);
                 const uint64_t dv0 = umma_desc_sw128(base + VF_OFF_V, VF_HALF_BYTES, 1024);
+                const uint64_t dp0 = umma_desc_sw128(base + VF_OFF_P, 16, 1024);
                 bool ok = true;
                 int jj = 0, ii = 0;
                 int pv_jj = -1, pv_ii = 0;
                 bool pv_first = false, pv_last = false;
-                auto do_pv = [&]() -> bool {       // O += P(pv_jj) V(pv_jj)
+                auto do_pv = [&]() -> bool {       // O^T += V(pv_jj)^T P(pv_jj)^T
                     if (!vf_wait(bar_p_full + (pv_jj & 1) * 8, (uint32_t)(pv_jj >> 1) & 1u, p.wait_ns, abort_flag))
                         return false;
                     if (!vf_wait(bar_v_full + (pv_jj % VF_VSTAGES) * 8, (uint32_t)(pv_jj / VF_VSTAGES) & 1u, p.wait_ns,
@@ -349,11 +364,12 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                         return false;
                     tc_fence_after();
                     const uint64_t dv = dv0 + (uint64_t)(((pv_jj % VF_VSTAGES) * VF_TILE_BYTES) >> 4);
-                    const uint32_t pcol = tmem + VF_COL_S + (pv_jj & 1) * 128;
+                    const uint64_t dp = dp0 + (uint64_t)(((pv_jj & 1) * VF_P_BYTES) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < VF_KT / 16; ++ks)
-                        umma_f16_tmem_a(tmem + VF_COL_O, pcol + ks * 8, dv + (uint64_t)((ks * 16 * 128) >> 4), idesc_o,
-                                        (ks > 0 || !pv_first) ? 1u : 0u);
+                        umma_f16(tmem + VF_COL_O, dv + (uint64_t)((ks * 16 * 128) >> 4),
+                                 dp + (uint64_t)(((ks >> 2) * PBLK + (ks & 3) * 32) >> 4), idesc_o,
+                                 (ks > 0 || !pv_first) ? 1u : 0u);
                     umma_commit(bar_v_empty + (pv_jj % VF_VSTAGES) * 8);
                     umma_commit(bar_pv_done + (pv_jj & 1) * 8);
                     if (pv_last) umma_commit(bar_o_full);
@@ -378,8 +394,9 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                             break;
                         consumed_k = jj + 1;
                         tc_fence_after();
-                        // S(jj) = Q4 K(jj)^T over the S/P buffer of tile jj; it is issued after P(jj-2).V, which read
-                        // that buffer (one thread's MMAs execute in order)
+                        // S(jj) = Q4 K(jj)^T into S buffer jj & 1; it is issued after P(jj-2).V, whose weights came
+                        // from that buffer and whose P^T buffer the softmax of tile jj rewrites (one thread's MMAs
+                        // execute in order, and the commit of S(jj) covers P(jj-2).V)
                         const uint64_t dk = dk0 + (uint64_t)(((jj % VF_KSTAGES) * VF_TILE_BYTES) >> 4);
                         const uint32_t scol = tmem + VF_COL_S + (jj & 1) * 128;
 #pragma unroll
@@ -405,12 +422,17 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         }
     } else {
         setmaxnreg_inc<VF_REGS_HIGH>();
-        // ---------------------------------------------------------------------- softmax + epilogue (copy `warp`)
-        const int slice = SPLIT_P ? (warp & 1) : warp;       // this copy's keys: [slice * SW, slice * SW + SW)
-        const bool lo_part = SPLIT_P && warp >= 2;           // writes the weights' low parts
+        // ---------------------------------------------------------------------- softmax of slice `warp`, epilogue
+        const int slice = warp;                              // keys [32 w, 32 w + 32) of every tile
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const int n = lane;                                  // query row (of the head group)
         const int qi = n < p.rows ? n / p.G : p.q_len - 1;
+        // this row's P^T rows (high parts: row n; low parts: row 32 + n) inside the slice's 64-key block, 128-byte
+        // swizzled: the 16-byte chunk j of a row lands at chunk j ^ (row & 7)
+        const uint32_t p_hi = base + VF_OFF_P + (slice >> 1) * PBLK + (n >> 3) * 1024 + (n & 7) * 128;
+        const uint32_t p_lo = p_hi + 4 * 1024;
+        const int chunk0 = (slice & 1) * 4;
+        const int n_qi = n < p.rows ? n / p.G : 0;         // query position of row n (0 for padding rows)
         int jj = 0, ii = 0;
         bool ok = true;
         VfItems items(p, nlaunch, n_items);
@@ -418,35 +440,42 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         while (ok && items.next(it)) {
             if (it.ntiles == 0) continue;
             const int lim = it.L - p.q_len + qi;              // last key this row sees
-            float m_ref = -INFINITY, l = 0.f;
+            float m_ref = -INFINITY, l = 0.f;                 // the row's reference max (all slices) and slice sum
             for (int t = 0; t < it.ntiles; ++t, ++jj) {
                 ok = __all_sync(0xffffffffu, vf_wait(bar_s_full + (jj & 1) * 8, (uint32_t)(jj >> 1) & 1u, p.wait_ns,
                                                      abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t scol = tmem + lane_base + VF_COL_S + (jj & 1) * 128;
-                float sv[SW];
-                tmem_ld_cols<SW>(scol + slice * SW, sv);
+                float sv[VF_SW];
+                tmem_ld_cols<VF_SW>(scol + slice * VF_SW, sv);
                 const int t0 = it.t_begin + t * VF_KT;
-                const int k0 = t0 + slice * SW;               // absolute index of the slice's first key
+                const int k0 = t0 + slice * VF_SW;            // absolute index of the slice's first key
                 const int nvalid = it.t_end - t0;             // keys of this tile inside the item (>= 1)
                 // last visible key of this row in the slice (keys past the item or the row's limit are masked)
                 const int cut = min(it.t_end - 1, lim) - k0;
                 float m4[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) m4[i] = -INFINITY;
-                if (cut >= SW - 1) {
+                if (cut >= VF_SW - 1) {
 #pragma unroll
-                    for (int c = 0; c < SW; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+                    for (int c = 0; c < VF_SW; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < SW; ++c) {
+                    for (int c = 0; c < VF_SW; ++c) {
                         sv[c] = c <= cut ? sv[c] : -INFINITY;
                         m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
                     }
                 }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+                // the tile's maximum of the row over all four slices
+                float *mrow = mxs + ((jj & 1) * VF_ROWS + n) * 4;
+                mrow[slice] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+                mbar_arrive(bar_mx);
                 __nanosleep(0);   // let the MMA warp of this sub-partition issue
+                ok = __all_sync(0xffffffffu, vf_wait(bar_mx, (uint32_t)jj & 1u, p.wait_ns, abort_flag));
+                if (!ok) break;
+                const float4 mv = *reinterpret_cast<const float4 *>(mrow);
+                const float mx = fmaxf(fmaxf(mv.x, mv.y), fmaxf(mv.z, mv.w));
                 float alpha = 1.f;
                 bool rescale = false;
                 if (mx > m_ref + VF_RESCALE_LOG2 || (m_ref == -INFINITY && mx > -INFINITY)) {
@@ -454,18 +483,20 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                     m_ref = mx;
                     rescale = true;
                 }
+                // every slice takes the same decision for a row, so the four warps agree on this vote
                 if (t > 0 && __any_sync(0xffffffffu, rescale)) {
-                    // O holds the item's P.V up to tile t-1: wait for that product, then rescale this copy's rows
+                    // O^T holds the item's P.V up to tile t-1: wait for that product, then rescale the columns of
+                    // the rows whose reference max moved (this warp's 32 dimensions of each)
                     ok = __all_sync(0xffffffffu, vf_wait(bar_pv_done + ((jj - 1) & 1) * 8,
                                                          (uint32_t)((jj - 1) >> 1) & 1u, p.wait_ns, abort_flag));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int c0 = 0; c0 < VF_D; c0 += 32) {
+                    for (int c0 = 0; c0 < NP; c0 += 32) {
                         float a[32];
                         tmem_ld32(tmem + lane_base + VF_COL_O + c0, a);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) a[c] *= alpha;
+                        for (int c = 0; c < 32; ++c) a[c] *= __shfl_sync(0xffffffffu, alpha, c);
                         tmem_st32(tmem + lane_base + VF_COL_O + c0, a);
                     }
                 }
@@ -474,44 +505,37 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) r4[i] = 0.f;
 #pragma unroll
-                for (int c = 0; c < SW; ++c) {
+                for (int c = 0; c < VF_SW; ++c) {
                     sv[c] = ex2_approx(fmaf(sv[c], p.scale_log2, nmuse));
                     r4[c & 3] += sv[c];
                     if ((c & 15) == 15) __nanosleep(0);
                 }
                 l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
-                // P4 row: 128 keys as 64 packed columns; this copy's slice holds its weights (the high or the low
-                // parts), the other slices zero
+                // the slice's weights into P^T buffer jj & 1 (its previous reader, P(jj-2).V, completed before S(jj))
                 {
-                    uint32_t wv[SW / 2];
+                    const uint32_t pb = (uint32_t)(jj & 1) * VF_P_BYTES;
 #pragma unroll
-                    for (int c = 0; c < SW / 2; ++c) {
-                        const float x0 = sv[2 * c], x1 = sv[2 * c + 1];
-                        wv[c] = pack2<T>(x0, x1);
-                        if (lo_part) {
-                            // a bf16 is the top half of an fp32
-                            const float h0 = __uint_as_float(wv[c] << 16), h1 = __uint_as_float(wv[c] & 0xFFFF0000u);
-                            wv[c] = pack2<T>(x0 - h0, x1 - h1);
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = sv[8 * j + 2 * e], x1 = sv[8 * j + 2 * e + 1];
+                            hw[e] = pack2<T>(x0, x1);
+                            if (SPLIT_P) {
+                                // a bf16 is the top half of an fp32
+                                const float h0 = __uint_as_float(hw[e] << 16), h1 = __uint_as_float(hw[e] & 0xFFFF0000u);
+                                lw[e] = pack2<T>(x0 - h0, x1 - h1);
+                            }
                         }
+                        const uint32_t off = pb + (uint32_t)(((chunk0 + j) ^ (n & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_hi + off), "r"(hw[0]),
+                                     "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
+                                     : "memory");
+                        if (SPLIT_P)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_lo + off), "r"(lw[0]),
+                                         "r"(lw[1]), "r"(lw[2]), "r"(lw[3])
+                                         : "memory");
                     }
-                    // the slice's packed columns lie in 32-column group g (fp16: in its low or high half)
-                    const int g = (slice * (SW / 2)) >> 5;
-                    uint32_t w[32];
-                    if constexpr (SW / 2 == 32) {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) w[c] = wv[c];
-                    } else {
-                        const bool upper = (slice & 1) != 0;
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            w[c] = upper ? 0u : wv[c];
-                            w[16 + c] = upper ? wv[c] : 0u;
-                        }
-                    }
-                    tmem_st32_raw(scol + 32 * g, w);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) w[c] = 0u;
-                    tmem_st32_raw(scol + 32 * (1 - g), w);
                 }
                 if (nvalid < VF_KT && warp == 0) {
                     // keys past the item: their V rows hold other data (possibly NaN): zero them once the tile has
@@ -527,74 +551,76 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                             *reinterpret_cast<uint4 *>(vt + VF_HALF_BYTES + c * 128 + k * 16) = make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
-                    fence_proxy_async_smem();
                 }
-                tmem_wait_st();
+                fence_proxy_async_smem();   // the weights (and zeroed V rows) are read by the tensor cores
                 tc_fence_before();
                 mbar_arrive(bar_p_full + (jj & 1) * 8);
             }
             if (!ok) break;
-            // ---- epilogue of the item: merge the copies (log-sum-exp weights), normalise, store
+            // ---- epilogue of the item: O^T column n is row n's unnormalised output (bf16: plus column 32 + n)
             ok = __all_sync(0xffffffffu, vf_wait(bar_o_full, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            float o[VF_D];
-            tmem_ld_cols<VF_D>(tmem + lane_base + VF_COL_O, o);
+            float oh[32], ol[32];
+            tmem_ld32(tmem + lane_base + VF_COL_O, oh);
+            if (SPLIT_P) tmem_ld32(tmem + lane_base + VF_COL_O + 32, ol);
             tc_fence_before();
             mbar_arrive(bar_o_free);
-            mlx[warp * VF_ROWS + n] = make_float2(m_ref, l);
-            mbar_arrive(bar_ml);
-            ok = __all_sync(0xffffffffu, vf_wait(bar_ml, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+            // the row's sum over the four slices
+            lsx[n * 4 + slice] = l;
+            mbar_arrive(bar_lx);
+            ok = __all_sync(0xffffffffu, vf_wait(bar_lx, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
             if (!ok) break;
-            {
-                float M = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < NSLICE; ++c) M = fmaxf(M, mlx[c * VF_ROWS + n].x);
-                const float Muse = M == -INFINITY ? 0.f : M;
-                float lsum = 0.f;
-#pragma unroll
-                for (int c = 0; c < NSLICE; ++c) {
-                    const float2 v = mlx[c * VF_ROWS + n];
-                    lsum += v.x == -INFINITY ? 0.f : ex2_approx(v.x - Muse) * v.y;
-                }
-                if (warp == 0) mlm[n] = make_float2(M, lsum);
-                // this copy's rows, scaled to the common max, into its staging rows
-                const float wown = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - Muse);
-                float *dst = stage + (warp * VF_ROWS + n) * VF_ST_STRIDE;
-#pragma unroll
-                for (int c = 0; c < VF_D; c += 4)
-                    *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c] * wown, o[c + 1] * wown, o[c + 2] * wown,
-                                                                       o[c + 3] * wown);
-            }
-            mbar_arrive(bar_st1);
-            ok = __all_sync(0xffffffffu, vf_wait(bar_st1, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
-            if (!ok) break;
-            // warp w sums the copies of rows 8w..8w+7 and stores them, one row per step, 4 dims per lane (every
-            // row is read and written as one contiguous run)
+            const float4 lv = *reinterpret_cast<const float4 *>(lsx + n * 4);
+            const float lsum = (lv.x + lv.y) + (lv.z + lv.w);
             {
                 const bool direct = p.part0 == 0 && it.L <= p.part_tokens;   // the merge skips such sequences
-#pragma unroll 1
-                for (int r = warp * 8; r < warp * 8 + 8 && r < p.rows; ++r) {
-                    float4 acc = *reinterpret_cast<const float4 *>(stage + r * VF_ST_STRIDE + 4 * lane);
+                if (!direct && warp == 0 && n < p.rows) {
+                    const int64_t orow_n = ((int64_t)it.b * p.q_len + n_qi) * p.Hq + it.g * p.G + (n - n_qi * p.G);
+                    p.part_ml[orow_n * p.max_parts + it.part] = make_float2(m_ref, lsum);
+                }
+                // the item's rows into shared memory (warp w: dimensions 32w..32w+31 of each row; the previous item's
+                // readers of these rows have all passed this item's sum exchange), then out in 16-byte stores (storing
+                // each warp's 64- or 128-byte piece of every row straight from registers took ~4,000 cycles an item
+                // on the shared-prefix verify workload, these few wide stores ~700)
+                float sc[VF_ROWS];
+                const float sc_n = direct ? 1.f / lsum : 1.f;
 #pragma unroll
-                    for (int c = 1; c < 4; ++c) {
-                        const float4 x = *reinterpret_cast<const float4 *>(stage + (c * VF_ROWS + r) * VF_ST_STRIDE + 4 * lane);
-                        acc.x += x.x;
-                        acc.y += x.y;
-                        acc.z += x.z;
-                        acc.w += x.w;
+                for (int r = 0; r < VF_ROWS; ++r) sc[r] = __shfl_sync(0xffffffffu, sc_n, r);
+                if (direct) {
+                    T *orows = reinterpret_cast<T *>(smem + VF_OFF_O);                 // [32][128] T
+#pragma unroll
+                    for (int r = 0; r < VF_ROWS; ++r)
+                        if (r < p.rows) orows[r * VF_D + 32 * warp + lane] = vf_round<T>((SPLIT_P ? oh[r] + ol[r] : oh[r]) * sc[r]);
+                } else {
+                    float *orows = reinterpret_cast<float *>(smem + VF_OFF_O);         // [32][128] fp32
+#pragma unroll
+                    for (int r = 0; r < VF_ROWS; ++r)
+                        if (r < p.rows) orows[r * VF_D + 32 * warp + lane] = SPLIT_P ? oh[r] + ol[r] : oh[r];
+                }
+                mbar_arrive(bar_ost);
+                ok = __all_sync(0xffffffffu, vf_wait(bar_ost, (uint32_t)ii & 1u, p.wait_ns, abort_flag));
+                if (!ok) break;
+                // row r is query position r / G, head g * G + r % G
+                const int64_t obase = ((int64_t)it.b * p.q_len) * p.Hq + it.g * p.G;
+                if (direct) {
+                    // 256-byte rows: half a warp per row, warp w takes rows 2w, 2w + 1, 2w + 8, 2w + 9, ...
+                    const int half = lane >> 4, c16 = lane & 15;
+#pragma unroll 1
+                    for (int r = 2 * warp + half; r < p.rows; r += 8) {
+                        const int rq = r / p.G;
+                        const int64_t orow = obase + (int64_t)rq * p.Hq + (r - rq * p.G);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(smem + VF_OFF_O + (r * VF_D) * sizeof(T) + 16 * c16);
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + orow * VF_D + 8 * c16) = v;
                     }
-                    const float2 ml = mlm[r];
-                    const int rqi = r / p.G;
-                    const int64_t orow = ((int64_t)it.b * p.q_len + rqi) * p.Hq + it.g * p.G + (r - rqi * p.G);
-                    if (direct) {
-                        const float inv = 1.f / ml.y;
-                        *reinterpret_cast<uint2 *>(reinterpret_cast<T *>(p.out) + orow * VF_D + 4 * lane) =
-                            make_uint2(pack2<T>(acc.x * inv, acc.y * inv), pack2<T>(acc.z * inv, acc.w * inv));
-                    } else {
-                        const int64_t prow = orow * p.max_parts + it.part;
-                        *reinterpret_cast<float4 *>(p.part_o + prow * VF_D + 4 * lane) = acc;
-                        if (lane == 0) p.part_ml[prow] = ml;
+                } else {
+                    // 512-byte partition-state rows: one warp per row
+#pragma unroll 1
+                    for (int r = warp; r < p.rows; r += 4) {
+                        const int rq = r / p.G;
+                        const int64_t orow = obase + (int64_t)rq * p.Hq + (r - rq * p.G);
+                        const float4 v = *reinterpret_cast<const float4 *>(smem + VF_OFF_O + (r * VF_D + 4 * lane) * 4);
+                        *reinterpret_cast<float4 *>(p.part_o + (orow * p.max_parts + it.part) * VF_D + 4 * lane) = v;
                     }
                 }
             }
