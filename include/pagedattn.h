@@ -315,15 +315,17 @@ int32_t pa_decode_launches(const pa_pool *pool, int32_t block_table_stride, int3
  * budget, or a latency-critical loop that must not make cudaMalloc's
  * synchronising call. Such a caller cannot create a pool, because
  * pa_pool_create allocates the split workspace. This entry point takes the
- * pool geometry directly and keeps its scratch (a status word and the split
- * workspace) in one static device array of PA_NOALLOC_SCRATCH_BYTES, which
+ * pool geometry directly and keeps its scratch (a status word, two work
+ * counters and the split workspace) in one static device array of PA_NOALLOC_SCRATCH_BYTES, which
  * every GPU that runs it holds from its first call until the process exits.
  * The pages have no counterpart to this entry point; it computes what
  * pa_decode computes, with the same decode and merge kernels.
  *
  *  - Inputs and outputs are the caller's, with pa_decode's layouts and meaning;
  *    num_blocks .. dtype and partition_tokens (0 = 512) are as in pa_pool_config.
- *  - Scratch needed: 256 bytes (the status word), plus, when P =
+ *  - Scratch needed: 256 bytes (the status word and the counters with which
+ *    the tensor-core kernel's CTAs share out their items; each launch leaves
+ *    them at zero), plus, when P =
  *    ceil(block_table_stride * block_size / partition_tokens) > 1,
  *    num_seqs * q_len * num_q_heads * P * head_dim * 4 bytes (rounded up to
  *    256) and num_seqs * q_len * num_q_heads * P * 8. A larger request returns

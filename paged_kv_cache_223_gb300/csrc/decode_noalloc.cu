@@ -12,7 +12,7 @@ using namespace pa;
 namespace {
 
 constexpr size_t SCRATCH_BYTES = PA_NOALLOC_SCRATCH_BYTES;
-constexpr size_t STATUS_BYTES = 256;   // the call's device status word, padded to keep the partials aligned
+constexpr size_t STATUS_BYTES = 256;   // the call's status word (offset 0) and item counters (offset 128), padded
 
 // The call's status word (bytes 0..3), then the split pass's workspace: partition outputs followed by
 // the (max, sum) pairs. Every call clears the status word and writes each partial slot it later reads.
@@ -161,6 +161,7 @@ extern "C" pa_status pa_decode_noalloc(const void *q, const void *k_cache, const
     p.context_lens = context_lens;
     p.k_scales = p.v_scales = nullptr;
     p.status = reinterpret_cast<int *>(sbase);
+    p.vf_work = reinterpret_cast<int *>(sbase + 128);   // tensor-core decode's item counters (each launch resets them)
     p.part_o = reinterpret_cast<float *>(sbase + STATUS_BYTES);
     p.part_ml = reinterpret_cast<float2 *>(sbase + STATUS_BYTES + o_bytes);
     p.stride = block_table_stride;

@@ -21,6 +21,7 @@ struct pa_pool {
     float2 *part_ml = nullptr;
     int64_t ws_slots = 0;        // (output row, partition) pairs the workspace holds
     int *status = nullptr;
+    int *work = nullptr;         // tensor-core decode's item counters (in the status allocation; reset by each launch)
     int sm_count = 0;
     int part_tokens = 512;
     uint64_t wait_ns = 2000000000ull;
@@ -177,11 +178,12 @@ pa_status pa_pool_create(const pa_pool_config *config, pa_pool **out) {
             return PA_ERR_OOM;
         }
     }
-    if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess || cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
+    if (cudaMalloc(&p->status, 64) != cudaSuccess || cudaMemset(p->status, 0, 64) != cudaSuccess) {
         cudaGetLastError();
         free_pool(p);
         return PA_ERR_OOM;
     }
+    p->work = p->status + 8;
     if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess) {
@@ -341,6 +343,7 @@ pa_status pa_decode(pa_pool *pool, const void *q, const void *k_cache, const voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, pool->cfg.head_dim, pool->sm_count);
     p.vf_ctas = pool->sm_count;
+    p.vf_work = pool->work;
     if (launch_decode(p, pool->cfg.dtype, pool->cfg.head_dim, tmk, tmv, s, kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1 && launch_merge(p, pool->cfg.dtype, pool->cfg.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
@@ -398,6 +401,8 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
     // prefix kernel), and the persistent tensor-core kernel's per-item epilogue outweighs its gain there
     // (shared-prefix verify workload: 0.127 vs 0.076 ms per call)
     p.allow_verify = false;
+    p.vf_ctas = pool->sm_count;
+    p.vf_work = pool->work;
     // the prefix kernel (tensor cores, one CTA per SM) goes first, straight onto the caller's stream, so
     // that its CTAs take whole SMs before the suffix decode (bandwidth, many small CTAs, on the pool's
     // side stream) fills the rest; the merge waits for both

@@ -47,6 +47,7 @@ struct DecodeParams {
     int merge_splits = 1;  // merge CTAs per (sequence, query position, KV head): each takes a share of
                            // the (row, 4-dim) columns, so small batches still fill the GPU
     int vf_ctas = 0;       // tensor-core verify kernel: persistent CTAs (0 = one per SM of the device)
+    int *vf_work = nullptr;  // tensor-core verify kernel: [next item, CTAs finished], both 0 between launches
     bool allow_verify = true;  // may route 9..32 rows to the tensor-core verify kernel
 };
 

@@ -24,14 +24,18 @@
 // O^T (each thread one dimension of every row) and coalesced row stores: no merge between warps.
 // K and V tiles are read from shared memory by the tensor cores once per tile each.
 //
-// One persistent CTA per SM walks its items (c, c + grid, ...); every role follows the same
-// sequence of tiles, so the copies of the next item start while the current one finishes.
+// One persistent CTA per SM takes items from a counter shared by the launch (its first item is its own
+// index; it holds at most two ahead of its copies, so CTAs that start late, beside another kernel, or run
+// short items take more); every role follows the same sequence of tiles, so the copies of the next item
+// start while the current one finishes.
 //   warps 0-3   softmax of key slice w (rows of quarter w), then the item's epilogue: warp w stores
 //               dimensions 32w..32w+31 of every row. Every sub-partition also hosts an issuing warp,
 //               and a warp scheduler that keeps picking a busy softmax warp starves it (an MMA issued
 //               from a sub-partition shared with one busy FP32 warp took 235 instead of 65 cycles),
 //               so the softmax yields its issue slot (nanosleep 0) every 16 exponentials.
 //   warp 4      MMA issue (one thread) and tensor-memory allocation.
+//   warp 5      item fetch (one thread): the next item and its sequence's context length into a ring
+//               that every role reads.
 //   warps 8-11  K producers, warps 12-15 V producers: each warp copies two 16-key sub-tiles of every
 //               tile, one TMA box per 64-dimension half; block ids looked up one tile ahead (one warp's
 //               copies are issued one after another, and TMA throughput scales with issuing warps).
@@ -55,20 +59,25 @@ constexpr int VF_OFF_V = VF_OFF_K + VF_KSTAGES * VF_TILE_BYTES;
 constexpr int VF_OFF_P = VF_OFF_V + VF_VSTAGES * VF_TILE_BYTES;    // P^T [2 buffers]
 constexpr int VF_OFF_O = VF_OFF_P + 2 * VF_P_BYTES;    // output rows of an item [32 rows][128 d] (fp32 or T)
 constexpr int VF_OFF_X = VF_OFF_O + VF_ROWS * VF_D * 4;   // slice maxima [2 tiles][32 rows][4], slice sums [32][4]
-constexpr int VF_OFF_BAR = VF_OFF_X + 3 * VF_ROWS * 4 * 4;
+constexpr int VF_QSLOTS = 8;                           // ring entries: items between the copies and the softmax
+constexpr int VF_LOOKAHEAD = 2;                        // items a CTA holds ahead of its copies (its current one included)
+constexpr int VF_OFF_RING = VF_OFF_X + 3 * VF_ROWS * 4 * 4;   // item ring: (item index or -1, context length)
+constexpr int VF_OFF_BAR = VF_OFF_RING + VF_QSLOTS * 8;
 // barriers: k_full[2] k_empty[2] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
-//           o_full o_free mx lx ost drain
-constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6;
-constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4]
+//           o_full o_free mx lx ost drain item_full[8] item_empty[8]
+constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6 + 2 * VF_QSLOTS;
+// roles that read every item of the ring: 4 K producer warps, 4 V producer warps, the MMA thread, 4 softmax warps
+constexpr int VF_ITEM_READERS = 13;
+constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4], items taken
 constexpr int VF_SMEM = 1024 + VF_OFF_MISC + 64;
 static_assert(VF_OFF_BAR % 8 == 0, "barrier alignment");
 static_assert(VF_SMEM <= 227 * 1024, "verify shared memory");
 
-// 16 warps; warps 5-7 only take part in the prologue and teardown. Launched at 128 registers per thread;
+// 16 warps; warp 5 fetches the CTA's items, warps 6-7 only take part in the prologue and teardown. Launched at 128 registers per thread;
 // the softmax warpgroup raises its share and the other three lower theirs (setmaxnreg):
 // 128 x 232 + 384 x 88 <= 512 x 128.
 constexpr int VF_THREADS = 512;
-constexpr int VF_MMA_WARP = 4, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
+constexpr int VF_MMA_WARP = 4, VF_SCHED_WARP = 5, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
 constexpr uint32_t VF_REGS_HIGH = 232, VF_REGS_LOW = 88;
 static_assert(128 * VF_REGS_HIGH + 384 * VF_REGS_LOW <= VF_THREADS * 128, "register split");
 // tensor memory: Q4[2] at columns 0 / 64 (128 d as 64 packed columns), S[2] at 128 / 256, O^T at 384 (64 columns)
@@ -129,6 +138,21 @@ __device__ __forceinline__ bool vf_wait(uint32_t bar, uint32_t parity, uint64_t 
     }
 }
 
+// Bounded wait until a counter another warp advances reaches `target` (or another role aborted).
+__device__ __forceinline__ bool vf_wait_count(volatile int *cnt, int target, uint64_t limit_ns, volatile int *abort_flag) {
+    if (*cnt >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(128);
+        if (*cnt >= target) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 struct VfItem {
     int idx;              // item index: (sequence, KV head, partition)
     int b, g, part, L;
@@ -136,25 +160,40 @@ struct VfItem {
     int ntiles;
 };
 
-// The CTA's items (idx = blockIdx.x, + gridDim.x, ...) in order. The next item's context length is
-// loaded one item ahead, so that no role waits on that load at an item boundary.
+// The CTA's items, in the order one thread of the CTA took them from the launch's shared counter (so
+// that CTAs which start late, or whose items are short, take more): every role reads the same ring of
+// (item, context length) entries and releases each entry once read. next() returns 1 for an item,
+// 0 at the end, -1 when the wait gave up (timeout or abort).
 struct VfItems {
     const DecodeParams &p;
-    int nlaunch, n_items, idx, Lnext;
+    const int2 *ring;
+    uint32_t full0, empty0;
+    volatile int *abort_flag;
+    int nlaunch, k;
+    bool whole_warp;   // all 32 lanes call next() (lane 0 releases the entry), else one thread
 
-    __device__ __forceinline__ VfItems(const DecodeParams &p_, int nlaunch_, int n_items_)
-        : p(p_), nlaunch(nlaunch_), n_items(n_items_), idx(blockIdx.x) {
-        Lnext = idx < n_items ? __ldg(p.context_lens + idx / nlaunch / p.Hkv) : 0;
-    }
+    __device__ __forceinline__ VfItems(const DecodeParams &p_, const int2 *ring_, uint32_t full0_, uint32_t empty0_,
+                                       volatile int *abort_, int nlaunch_, bool whole_warp_)
+        : p(p_), ring(ring_), full0(full0_), empty0(empty0_), abort_flag(abort_), nlaunch(nlaunch_), k(0),
+          whole_warp(whole_warp_) {}
 
-    __device__ __forceinline__ bool next(VfItem &it) {
-        if (idx >= n_items) return false;
+    __device__ __forceinline__ int next(VfItem &it) {
+        const int slot = k % VF_QSLOTS;
+        bool got = vf_wait(full0 + slot * 8, (uint32_t)(k / VF_QSLOTS) & 1u, p.wait_ns, abort_flag);
+        if (whole_warp) got = __all_sync(0xffffffffu, got);
+        if (!got) return -1;
+        const volatile int *e = reinterpret_cast<const volatile int *>(ring + slot);
+        const int idx = e[0], Lraw = e[1];
+        if (whole_warp) __syncwarp();
+        if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(empty0 + slot * 8);
+        ++k;
+        if (idx < 0) return 0;
         it.idx = idx;
         it.part = p.part0 + idx % nlaunch;
         const int bg = idx / nlaunch;
         it.g = bg % p.Hkv;
         it.b = bg / p.Hkv;
-        const int L = Lnext < 0 ? 0 : (Lnext > p.max_ctx ? p.max_ctx : Lnext);
+        const int L = Lraw < 0 ? 0 : (Lraw > p.max_ctx ? p.max_ctx : Lraw);
         it.L = L;
         const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
         it.t_begin = it.part * p.part_tokens;
@@ -165,9 +204,7 @@ struct VfItems {
             it.t_end = min(it.t_begin + p.part_tokens, L);
             it.ntiles = (it.t_end - it.t_begin + VF_KT - 1) / VF_KT;
         }
-        idx += gridDim.x;
-        if (idx < n_items) Lnext = __ldg(p.context_lens + idx / nlaunch / p.Hkv);
-        return true;
+        return 1;
     }
 };
 
@@ -197,9 +234,13 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     const uint32_t bar_lx = bar_mx + 8;
     const uint32_t bar_ost = bar_lx + 8;
     const uint32_t bar_drain = bar_ost + 8;
+    const uint32_t bar_item_full = bar_drain + 8;
+    const uint32_t bar_item_empty = bar_item_full + VF_QSLOTS * 8;
+    int2 *item_ring = reinterpret_cast<int2 *>(smem + VF_OFF_RING);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + VF_OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *issued = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [K warps 0..3, V warps 0..3]
+    volatile int *taken = reinterpret_cast<volatile int *>(tmem_slot + 10);   // ring entries the copies have started
     float *mxs = reinterpret_cast<float *>(smem + VF_OFF_X);                   // [2 tiles][32 rows][4 slices]
     float *lsx = mxs + 2 * VF_ROWS * 4;                                        // [32 rows][4 slices]
 
@@ -231,8 +272,13 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         mbar_init(bar_lx, 128);
         mbar_init(bar_ost, 128);
         mbar_init(bar_drain, 1);
+        for (int s = 0; s < VF_QSLOTS; ++s) {
+            mbar_init(bar_item_full + s * 8, 1);
+            mbar_init(bar_item_empty + s * 8, VF_ITEM_READERS);
+        }
         *abort_flag = 0;
         for (int i = 0; i < 8; ++i) issued[i] = 0;
+        *taken = 0;
         fence_barrier_init();
     }
     tc_fence_before();
@@ -259,9 +305,15 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
             const int qn = lane, qqi = qn < p.rows ? qn / p.G : 0, qhh = qn - qqi * p.G;
             int jj = 0, ii = 0;
             bool ok = true;
-            VfItems items(p, nlaunch, n_items);
+            VfItems items(p, item_ring, bar_item_full, bar_item_empty, abort_flag, nlaunch, true);
             VfItem it;
-            while (ok && items.next(it)) {
+            while (ok) {
+                const int got = items.next(it);
+                if (got <= 0) {
+                    ok = got == 0;
+                    break;
+                }
+                if (!is_v && pw == 0 && lane == 0) *taken = items.k;   // lets the fetch take the next item
                 if (!is_v && pw == 0 && it.part == p.part0) {
                     const int Lraw = __ldg(p.context_lens + it.b);
                     if ((Lraw < p.q_len || Lraw > p.max_ctx) && lane == 0) set_status(p.status, STATUS_BOUNDS);
@@ -375,9 +427,14 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                     if (pv_last) umma_commit(bar_o_full);
                     return true;
                 };
-                VfItems items(p, nlaunch, n_items);
+                VfItems items(p, item_ring, bar_item_full, bar_item_empty, abort_flag, nlaunch, false);
                 VfItem it;
-                while (ok && items.next(it)) {
+                while (ok) {
+                    const int got = items.next(it);
+                    if (got <= 0) {
+                        ok = got == 0;
+                        break;
+                    }
                     if (it.ntiles == 0) continue;
                     if (!(ok = vf_wait(bar_q_full + (ii & 1) * 8, (uint32_t)(ii >> 1) & 1u, p.wait_ns, abort_flag)))
                         break;
@@ -419,6 +476,29 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                 if (!ok) *abort_flag = 1;
             }
             __syncwarp();
+        } else if (warp == VF_SCHED_WARP) {
+            // ------------------------------------------------------------------ item fetch (lane 0)
+            // the CTA's first item is its own index; each later one comes from the launch's shared counter, taken
+            // only once the copies have started the item before it (a CTA reserves at most VF_LOOKAHEAD items, so
+            // CTAs that start late or run short items take more); with it goes its sequence's context length.
+            // -1 marks the end.
+            if (lane == 0) {
+                for (int k = 0;; ++k) {
+                    const int slot = k % VF_QSLOTS;
+                    if (k >= VF_QSLOTS && !vf_wait(bar_item_empty + slot * 8, (uint32_t)((k / VF_QSLOTS) - 1) & 1u,
+                                                   p.wait_ns, abort_flag, 256))
+                        break;
+                    if (k >= VF_LOOKAHEAD && !vf_wait_count(taken, k - VF_LOOKAHEAD + 1, p.wait_ns, abort_flag)) break;
+                    int idx = k == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.vf_work, 1);
+                    int L = 0;
+                    if (idx >= n_items) idx = -1;
+                    else L = __ldg(p.context_lens + idx / nlaunch / p.Hkv);
+                    item_ring[slot] = make_int2(idx, L);
+                    mbar_arrive(bar_item_full + slot * 8);
+                    if (idx < 0) break;
+                }
+            }
+            __syncwarp();
         }
     } else {
         setmaxnreg_inc<VF_REGS_HIGH>();
@@ -435,9 +515,14 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         const int n_qi = n < p.rows ? n / p.G : 0;         // query position of row n (0 for padding rows)
         int jj = 0, ii = 0;
         bool ok = true;
-        VfItems items(p, nlaunch, n_items);
+        VfItems items(p, item_ring, bar_item_full, bar_item_empty, abort_flag, nlaunch, true);
         VfItem it;
-        while (ok && items.next(it)) {
+        while (ok) {
+            const int got = items.next(it);
+            if (got <= 0) {
+                ok = got == 0;
+                break;
+            }
             if (it.ntiles == 0) continue;
             const int lim = it.L - p.q_len + qi;              // last key this row sees
             float m_ref = -INFINITY, l = 0.f;                 // the row's reference max (all slices) and slice sum
@@ -655,6 +740,14 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, VF_TMEM_COLS);
     }
+    if (tid == 0) {
+        // the last CTA to finish (every CTA has taken its last item by then) resets the counters for the next launch
+        __threadfence();
+        if (atomicAdd(p.vf_work + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(p.vf_work, 0);
+            atomicExch(p.vf_work + 1, 0);
+        }
+    }
 }
 
 template <typename T>
@@ -668,7 +761,7 @@ static cudaError_t launch_verify_t(const DecodeParams &p, const CUtensorMap &tmk
 
 cudaError_t launch_verify(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                           int max_ctas, cudaStream_t stream) {
-    if (p.rows < 1 || p.rows > VF_ROWS) return cudaErrorInvalidValue;
+    if (p.rows < 1 || p.rows > VF_ROWS || p.vf_work == nullptr) return cudaErrorInvalidValue;
     const int64_t items = (int64_t)p.num_seqs * p.Hkv * (p.max_parts - p.part0);
     const int grid = (int)(items < max_ctas ? items : max_ctas);
     if (grid < 1) return cudaSuccess;
