@@ -735,10 +735,10 @@ static cudaError_t launch_decode_d(const DecodeParams &p, const CUtensorMap &tmk
 }
 
 // The tensor-core kernel of verify.cu takes 16-bit pools with head_dim 128 when a KV head has more than one
-// 8-column MMA tile of query rows here (9..32 rows). Measured against this kernel: 1.58x for the 70B-shaped
-// 4-draft verify (32 rows, 8192 tokens), 1.45x for 32 fp16 rows at 4096 tokens, 1.33x for a 32-head group at
-// 32768 tokens, 1.13x for 20 rows (q_len 5, G 4) at 8192 tokens, 1.02x on the shared-prefix verify workload,
-// equal for 128 sequences of 1088..1536 tokens.
+// 8-column MMA tile of query rows here (9..32 rows). Measured against this kernel: 1.45x for the 70B-shaped
+// 4-draft verify (32 rows, 8192 tokens), 1.48x for 32 fp16 rows at 4096 tokens, 1.37x for a 32-head group at
+// 32768 tokens, 1.16x for 20 rows (q_len 5, G 4) at 8192 tokens, 1.13x on the shared-prefix verify workload,
+// 1.04x for 128 sequences of 1088..1536 tokens, 0.98x for 12 rows at 2000 tokens.
 bool decode_uses_verify(int head_dim, int rows, bool kv8) { return !kv8 && head_dim == 128 && rows > 8; }
 
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,

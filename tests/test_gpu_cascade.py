@@ -22,6 +22,8 @@ CASES = [
     ([4, 64, 1000], 8, 8, 16, 4, synth.BF16, 1536, 512),            # MHA (G = 1), 3 prefix partitions
     ([2, 257, 31], 16, 4, 32, 2, synth.FP16, 768, 256),             # bs 32, 256-token partitions
     ([5, 5, 6, 7], 24, 8, 16, 5, synth.FP16, 512, 512),             # G = 3 (15 rows), suffix == q_len
+    ([3, 90, 700], 24, 4, 16, 3, synth.BF16, 1536, 512),            # 18 rows, 3 prefix partitions
+    ([10, 300, 4], 32, 8, 32, 4, synth.FP16, 1280, 256),            # 16 rows, bs 32, 5 prefix partitions
 ]
 
 
