@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     const int lane = threadIdx.x & 31;
     const int nlaunch = p.max_parts - p.part0;         // partitions launched per (sequence, KV head)
     const int part = p.part0 + (int)(blockIdx.x % nlaunch);
+    // launched with programmatic serialization: the merge behind this kernel may be launched now (its CTAs
+    // take only what this grid leaves free and wait for its end); this kernel waits for the work ahead of it
+    pdl_trigger();
+    pdl_wait();
     const int bg = blockIdx.x / nlaunch;
     const int g = bg % p.Hkv;
     const int b = bg / p.Hkv;
@@ -566,6 +570,7 @@ __host__ __device__ inline int merge_threads(int pairs, int max_parts) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams p) {
+    pdl_wait();   // the partitions' states are written by the kernel ahead of this one
     extern __shared__ float msm[];                 // weights [G][max_parts], den [G], sums [groups][pairs]
     const int unit = blockIdx.x / p.merge_splits;  // (b, qi, g)
     const int split = blockIdx.x - unit * p.merge_splits;
@@ -663,6 +668,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const DecodeParams p) {
     static_assert(D % 32 == 0 && D / 32 <= 4, "dims per lane");
     constexpr int DL = D / 32;                     // dims per lane
+    pdl_wait();   // the partitions' states are written by the kernel ahead of this one
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * MERGE_ROW_WARPS + warp;   // (b * q_len + qi) * Hq + h
     if (row >= (int64_t)p.num_seqs * p.q_len * p.Hq) return;
@@ -718,8 +724,8 @@ static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tmk
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)p.num_seqs * p.Hkv * (p.max_parts - p.part0);
-    decode_kernel<T, D, NT, KV8><<<(unsigned)grid, DECODE_WARPS * 32, smem, stream>>>(tmk, tmv, p);
-    return cudaGetLastError();
+    e = launch_pdl(decode_kernel<T, D, NT, KV8>, dim3((unsigned)grid), dim3(DECODE_WARPS * 32), smem, stream, tmk, tmv, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int D, bool KV8>
@@ -784,28 +790,29 @@ int merge_splits_for(int64_t units, int G, int head_dim, int sm_count) {
     return want < 1 ? 1 : (int)want;
 }
 
-cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream) {
+cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream, bool pdl) {
+    cudaError_t e = cudaSuccess;
     if (p.max_parts <= 32) {
         const int64_t rows = (int64_t)p.num_seqs * p.q_len * p.Hq;
         const unsigned grid = (unsigned)((rows + MERGE_ROW_WARPS - 1) / MERGE_ROW_WARPS);
         if (dtype == PA_FP16) {
-            if (head_dim == 128) merge_rows_kernel<__half, 128><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
-            else merge_rows_kernel<__half, 64><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+            if (head_dim == 128) e = launch_maybe_pdl(pdl, merge_rows_kernel<__half, 128>, dim3(grid), dim3(MERGE_ROW_WARPS * 32), 0, stream, p);
+            else e = launch_maybe_pdl(pdl, merge_rows_kernel<__half, 64>, dim3(grid), dim3(MERGE_ROW_WARPS * 32), 0, stream, p);
         } else {
-            if (head_dim == 128) merge_rows_kernel<__nv_bfloat16, 128><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
-            else merge_rows_kernel<__nv_bfloat16, 64><<<grid, MERGE_ROW_WARPS * 32, 0, stream>>>(p);
+            if (head_dim == 128) e = launch_maybe_pdl(pdl, merge_rows_kernel<__nv_bfloat16, 128>, dim3(grid), dim3(MERGE_ROW_WARPS * 32), 0, stream, p);
+            else e = launch_maybe_pdl(pdl, merge_rows_kernel<__nv_bfloat16, 64>, dim3(grid), dim3(MERGE_ROW_WARPS * 32), 0, stream, p);
         }
-        return cudaGetLastError();
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     const int64_t units = (int64_t)p.num_seqs * p.q_len * p.Hkv * p.merge_splits;
     const size_t smem = merge_smem_bytes(p.G, p.max_parts, head_dim, p.merge_splits);
     const int pps = (p.G * (head_dim / 4) + p.merge_splits - 1) / p.merge_splits;
     const int threads = merge_threads(pps, p.max_parts);
-    cudaError_t e = cudaSuccess;
 #define PA_MERGE(TT, DD)                                                                                       \
     e = cudaFuncSetAttribute(merge_kernel<TT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (e != cudaSuccess) return e;                                                                            \
-    merge_kernel<TT, DD><<<(unsigned)units, threads, smem, stream>>>(p);
+    e = launch_maybe_pdl(pdl, merge_kernel<TT, DD>, dim3((unsigned)units), dim3(threads), smem, stream, p);             \
+    if (e != cudaSuccess) return e;
     if (dtype == PA_FP16) {
         if (head_dim == 128) { PA_MERGE(__half, 128) } else { PA_MERGE(__half, 64) }
     } else {

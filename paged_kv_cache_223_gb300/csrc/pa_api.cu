@@ -415,7 +415,7 @@ pa_status pa_decode_shared_prefix(pa_pool *pool, const void *q, const void *k_ca
     if (cudaEventRecord(pool->ev_join, pool->side) != cudaSuccess || cudaStreamWaitEvent(s, pool->ev_join, 0) != cudaSuccess)
         return PA_ERR_CUDA;
     p.merge_splits = merge_splits_for((int64_t)num_seqs * q_len * p.Hkv, p.G, c.head_dim, pool->sm_count);
-    if (launch_merge(p, c.dtype, c.head_dim, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_merge(p, c.dtype, c.head_dim, s, false) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
 

@@ -336,6 +336,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch (a kernel launched with programmatic stream serialization may start
+// before the kernel ahead of it in the stream has finished): pdl_wait() blocks until that kernel has
+// completed and its memory operations are visible, so it must precede any read of memory that work
+// earlier in the stream may write; pdl_trigger() lets the kernel behind this one be launched (its
+// threads then wait in their own pdl_wait()). Both are no-ops for a kernel launched normally.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(int *status, int bit) {
     if (status) atomicOr(status, bit);
 }

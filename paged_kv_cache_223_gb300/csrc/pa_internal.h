@@ -65,6 +65,32 @@ struct CacheWriteParams {
     int64_t num_blocks;
 };
 
+// A kernel launch with programmatic stream serialization: the kernel may be launched while the one ahead
+// of it in the stream is still running, and waits for it (pdl_wait) before touching memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_maybe_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args &&...args) {
+    if (pdl) return launch_pdl(kernel, grid, block, smem, stream, static_cast<Args &&>(args)...);
+    kernel<<<grid, block, smem, stream>>>(static_cast<Args &&>(args)...);
+    return cudaGetLastError();
+}
+
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_cache_write(const CacheWriteParams &p, int sm_count, cudaStream_t stream);
 // FP8 pools: k, v hold 16-bit rows of the model dtype; caches are codes followed by scales.
@@ -73,7 +99,9 @@ cudaError_t launch_cache_write_fp8(const void *k, const void *v, const int64_t *
                                    int *status, int sm_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, const CUtensorMap &tmk,
                           const CUtensorMap &tmv, cudaStream_t stream, bool kv8 = false);
-cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream);
+// pdl: launched with programmatic serialization behind the decode kernel that writes the partitions' states
+// (false when other work is ordered in between, e.g. an event wait)
+cudaError_t launch_merge(const DecodeParams &p, int dtype, int head_dim, cudaStream_t stream, bool pdl = true);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_spec_verify(const float *p, const float *q, const int32_t *draft, const float *u, const float *v,
                                int B, int K, int64_t V, int32_t *out, int32_t *n_out, int *status,

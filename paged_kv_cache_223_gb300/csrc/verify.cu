@@ -245,6 +245,10 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     float *lsx = mxs + 2 * VF_ROWS * 4;                                        // [32 rows][4 slices]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // launched with programmatic serialization: the merge behind this kernel may be launched now (its CTAs wait
+    // for this grid's end); this kernel waits for the work ahead of it before reading anything
+    pdl_trigger();
+    pdl_wait();
     const int nlaunch = p.max_parts - p.part0;
     const int n_items = p.num_seqs * p.Hkv * nlaunch;
 
@@ -755,8 +759,8 @@ static cudaError_t launch_verify_t(const DecodeParams &p, const CUtensorMap &tmk
                                    cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(verify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, VF_SMEM);
     if (e != cudaSuccess) return e;
-    verify_kernel<T><<<(unsigned)grid, VF_THREADS, VF_SMEM, stream>>>(tmk, tmv, p);
-    return cudaGetLastError();
+    e = launch_pdl(verify_kernel<T>, dim3((unsigned)grid), dim3(VF_THREADS), VF_SMEM, stream, tmk, tmv, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_verify(const DecodeParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
