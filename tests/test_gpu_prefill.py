@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from paged_kv_cache_223_gb300 import pagedattn as pa
 
@@ -55,6 +56,35 @@ def test_prefill_stress(stress):
     _, _, _, out = run_prefill(wl)
     ref, _, _ = H.oracle_reference(wl, 0)
     H.assert_close(out, ref, f"prefill {stress}")
+
+
+def _bf16_words(f: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 words, rounded to nearest even (test-side: builds inputs, not expected values)."""
+    u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_prefill_bf16_values_beyond_fp16_range():
+    """bf16 V values far outside fp16's range (where an fp16 shortcut for the weights would overflow): one
+    sequence's key tile 1 holds values near 3e5, the other's tile 4 (partly, up to its context end) values near
+    -1e5, the rest N(0,1)."""
+    wl = synth.custom_workload([700, 1300], 32, 8, 128, 16, 256, synth.BF16, tag=321)
+    pool, kc, vc, q, tables, lens = H.build_device(wl)
+    _, hk, hv = H.oracle_reference(wl, 0)
+    vw = vc.view(torch.int16)
+    for b, t0, t1, shift in ((1, 128, 256, 3.0e5), (0, 512, 700, -1.0e5)):
+        slots = wl.slots(b, np.arange(t0, t1))
+        blk, off = slots // wl.bs, slots % wl.bs
+        vals = (hv[blk, :, off, :].astype(np.uint32) << 16).view(np.float32) + np.float32(shift)
+        words = _bf16_words(vals)
+        hv[blk, :, off, :] = words
+        vw[torch.from_numpy(blk).to(H.DEV), :, torch.from_numpy(off).to(H.DEV), :] = \
+            torch.from_numpy(words.view(np.int16)).to(H.DEV)
+    out = pool.prefill(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _ = oracle.paged_attention(wl.q_values(0), hk, hv, wl.block_tables, wl.context_lens, wl.dtype, wl.scale)
+    assert np.abs(ref).max() > 1e4
+    H.assert_close(out, ref, "prefill with V beyond fp16's range")
 
 
 def test_prefill_matches_decode_for_short_chunks():
