@@ -66,6 +66,27 @@ def test_shared_prefix_equals_duplicated_bitwise():
     assert torch.equal(out_s, out_p)
 
 
+def test_inputs_written_just_before_the_call_are_seen():
+    """A kernel that writes the decode's query right before the call on the same stream, with no synchronisation in
+    between, is seen: the decode kernels may be launched while it runs (programmatic stream serialization), but they
+    wait for it before reading. A long kernel ahead of the write keeps it pending when the decode is launched."""
+    for wl in (synth.custom_workload([3000, 700, 4100], 64, 8, 128, 16, 1, synth.FP16, tag=51),   # 8 rows: decode + merge
+               synth.custom_workload([2000, 900], 32, 8, 128, 16, 5, synth.BF16, tag=52)):      # 20 rows: tensor-core kernel
+        pool, kc, vc, q, tables, lens = H.build_device(wl)
+        q2 = torch.flip(q, dims=[-1]).contiguous()
+        ref = pool.decode(q2, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+        torch.cuda.synchronize()
+        qq = q.clone()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        qq.copy_(q2)
+        out = pool.decode(qq, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
+        torch.cuda.synchronize()
+        assert pool.check() == pa.PA_OK
+        assert not torch.equal(ref, pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc))
+        assert torch.equal(out, ref)
+
+
 def test_deterministic_run_to_run():
     wl = synth.workload(5, batch=2)
     out, (pool, kc, vc, q, tables, lens) = _decode(wl)
