@@ -12,13 +12,17 @@ number generators", OOPSLA 2014):
     base     = mix(seed XOR (stream * 0xD1B54A32D192ED03))
     h(i)     = mix(base + i)                         (all arithmetic mod 2**64)
 
-Value recipe (an Irwin-Hall sum of four 16-bit uniforms, centred and scaled
-to unit variance; every step is an exactly rounded IEEE operation, so the host
-and the device produce the same bits):
-    s   = sum of the four 16-bit fields of h(i)      (integer in [0, 262140])
-    z   = float32(2*s - 262140) * C                  (C = float32 bits 0x375db3d7 = sqrt(3)/2**17)
+Value recipe (an Irwin-Hall sum of twelve 16-bit uniforms, centred: the classic
+"twelve uniforms minus six" stand-in for N(0,1), unit variance, tails out to 6 sigma;
+every step is an exactly rounded IEEE operation, so the host and the device produce
+the same bits):
+    s   = sum of the four 16-bit fields of each of h(3i), h(3i+1), h(3i+2)
+                                                     (integer in [0, 786420])
+    z   = float32(2*s - 786420) * 2**-17             (exact: |2s - 786420| < 2**20)
     x   = z * sigma + mean                           (two float32 operations, not fused)
     out = round-to-nearest-even of x to fp16 or bf16
+Each 16-bit field has variance (2**32 - 1)/12, so 2s - 786420 has variance
+4 (2**32 - 1) and z has variance 1 - 2**-32.
 
 synth/csrc/synth.cu implements the same definitions on the device for
 workloads too large to draw on the host; the two agree bit for bit.
@@ -39,8 +43,9 @@ GAMMA = 0x9E3779B97F4A7C15
 STREAM_MUL = 0xD1B54A32D192ED03
 M1 = 0xBF58476D1CE4E5B9
 M2 = 0x94D049BB133111EB
-C_BITS = 0x375DB3D7                       # float32(sqrt(3) / 2**17)
-C_F32 = np.array([C_BITS], dtype=np.uint32).view(np.float32)[0]
+N_HASH = 3                                # hashes (four 16-bit fields each) per value
+S_MAX = N_HASH * 4 * 0xFFFF               # largest field sum, 786420
+SCALE_F32 = np.float32(2.0 ** -17)        # 1 / sqrt(Var(2s - S_MAX)) up to 2**-33 relative
 
 FP16, BF16 = 0, 1
 DTYPES = {"fp16": FP16, "bf16": BF16}
@@ -79,11 +84,15 @@ def hash64(seed: int, stream: int, idx) -> np.ndarray:
 
 def unit_f32(seed: int, stream: int, idx, sigma: float = 1.0, mean: float = 0.0) -> np.ndarray:
     """The float32 value x of the recipe for each counter in idx."""
-    h = hash64(seed, stream, idx)
+    idx = np.asarray(idx, dtype=np.uint64)
     m16 = np.uint64(0xFFFF)
-    s = (h & m16) + ((h >> np.uint64(16)) & m16) + ((h >> np.uint64(32)) & m16) + (h >> np.uint64(48))
-    num = (2 * s.astype(np.int64) - 262140).astype(np.float32)
-    z = num * C_F32
+    s = np.zeros(idx.shape, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        for j in range(N_HASH):
+            h = hash64(seed, stream, idx * np.uint64(N_HASH) + np.uint64(j))
+            s += (h & m16) + ((h >> np.uint64(16)) & m16) + ((h >> np.uint64(32)) & m16) + (h >> np.uint64(48))
+    num = (2 * s.astype(np.int64) - S_MAX).astype(np.float32)
+    z = num * SCALE_F32
     z = z * np.float32(sigma)
     z = z + np.float32(mean)
     return z

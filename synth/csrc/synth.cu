@@ -1,7 +1,7 @@
 // synth.cu -- device-side copy of the seeded input generator in synth/__init__.py.
 //
 // Test and benchmark infrastructure: it fills buffers with the same 16-bit words the
-// host generator produces (SplitMix64 counter hash; Irwin-Hall sum of four 16-bit
+// host generator produces (SplitMix64 counter hash; Irwin-Hall sum of twelve 16-bit
 // fields; float32 scale; round to nearest even to fp16/bf16), so workloads of many GB
 // can be created on the GPU while the oracle regenerates any part of them on the host.
 // It holds none of the attention arithmetic.
@@ -19,11 +19,15 @@ __host__ __device__ __forceinline__ uint64_t mix(uint64_t z) {
 }
 
 __device__ __forceinline__ uint16_t value16(uint64_t base, uint64_t idx, int dtype, float sigma, float mean) {
-    const uint64_t h = mix(base + idx);
-    const uint32_t s = (uint32_t)(h & 0xFFFF) + (uint32_t)((h >> 16) & 0xFFFF) + (uint32_t)((h >> 32) & 0xFFFF) +
-                       (uint32_t)(h >> 48);
-    const float num = (float)(2 * (int32_t)s - 262140);           // exact
-    float z = __fmul_rn(num, __uint_as_float(0x375DB3D7u));        // sqrt(3) / 2^17
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {   // h(3i), h(3i+1), h(3i+2): twelve 16-bit fields
+        const uint64_t h = mix(base + 3 * idx + j);
+        s += (uint32_t)(h & 0xFFFF) + (uint32_t)((h >> 16) & 0xFFFF) + (uint32_t)((h >> 32) & 0xFFFF) +
+             (uint32_t)(h >> 48);
+    }
+    const float num = (float)(2 * (int32_t)s - 786420);           // exact
+    float z = __fmul_rn(num, 0x1p-17f);                            // exact: a power of two
     z = __fmul_rn(z, sigma);
     z = __fadd_rn(z, mean);
     if (dtype == 0) return __half_as_ushort(__float2half_rn(z));

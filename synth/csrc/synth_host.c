@@ -1,6 +1,6 @@
 /*
  * synth_host.c -- host-side, multithreaded copy of the seeded input generator defined in
- * synth/__init__.py (SplitMix64 counter hash; Irwin-Hall sum of four 16-bit fields;
+ * synth/__init__.py (SplitMix64 counter hash; Irwin-Hall sum of twelve 16-bit fields;
  * float32 scale; round to nearest even to fp16/bf16). Test and benchmark infrastructure:
  * it exists because the numpy statement of the recipe is too slow for multi-GB inputs.
  * It holds none of the attention arithmetic.
@@ -33,15 +33,15 @@ static uint16_t to_f16(float x) {
 }
 
 static uint16_t value16(uint64_t base, uint64_t idx, int dtype, float sigma, float mean) {
-    const uint64_t h = mix(base + idx);
-    const uint32_t s = (uint32_t)(h & 0xFFFF) + (uint32_t)((h >> 16) & 0xFFFF) + (uint32_t)((h >> 32) & 0xFFFF) +
-                       (uint32_t)(h >> 48);
-    const float num = (float)(2 * (int32_t)s - 262140);
-    uint32_t cb = 0x375DB3D7u;
-    float c;
-    memcpy(&c, &cb, 4);
-    /* three separately rounded float32 operations (built with -ffp-contract=off) */
-    float z = num * c;
+    uint32_t s = 0;
+    for (int j = 0; j < 3; ++j) { /* h(3i), h(3i+1), h(3i+2): twelve 16-bit fields */
+        const uint64_t h = mix(base + 3 * idx + (uint64_t)j);
+        s += (uint32_t)(h & 0xFFFF) + (uint32_t)((h >> 16) & 0xFFFF) + (uint32_t)((h >> 32) & 0xFFFF) +
+             (uint32_t)(h >> 48);
+    }
+    const float num = (float)(2 * (int32_t)s - 786420);   /* exact */
+    /* three separately rounded float32 operations (built with -ffp-contract=off); the first is exact */
+    float z = num * 0x1p-17f;
     z = z * sigma;
     z = z + mean;
     return dtype == 0 ? to_f16(z) : to_bf16(z);

@@ -17,14 +17,39 @@ def test_splitmix64_reference_values():
     assert [int(x) for x in h] == [synth._mix_py((base + i) & synth.MASK64) for i in range(4)]
 
 
-def test_scale_constant():
-    assert float(synth.C_F32) == float(np.float32(np.sqrt(3.0) / 131072.0))
+def test_scale_makes_unit_variance_exactly():
+    # Var of one 16-bit uniform field is (2**32 - 1)/12; twelve of them, doubled and scaled by 2**-17
+    # give 4 * 12 * (2**32 - 1) / 12 * 2**-34 = 1 - 2**-32.
+    var_field = ((1 << 32) - 1) / 12.0
+    assert synth.N_HASH * 4 == 12 and synth.S_MAX == 12 * 0xFFFF
+    assert abs(4 * 12 * var_field * float(synth.SCALE_F32) ** 2 - 1.0) < 1e-9
+    # |2s - S_MAX| < 2**20 and the scale is a power of two: z is exact in float32
+    assert synth.S_MAX < (1 << 20) and float(synth.SCALE_F32) == 2.0 ** -17
+
+
+def test_value_is_the_twelve_field_sum():
+    # brute force for a few counters, straight from the recipe's definition
+    base = synth.stream_base(3, 4)
+    for i in (0, 1, 77, (1 << 40) + 5):
+        s = 0
+        for j in range(3):
+            h = synth._mix_py((base + 3 * i + j) & synth.MASK64)
+            s += sum((h >> (16 * f)) & 0xFFFF for f in range(4))
+        want = np.float32((2 * s - 786420) / 131072.0)
+        assert synth.unit_f32(3, 4, np.array([i], dtype=np.uint64))[0] == want
 
 
 def test_values_moments_and_determinism():
-    x = synth.unit_f32(5, 11, np.arange(1 << 20, dtype=np.uint64))
+    x = synth.unit_f32(5, 11, np.arange(1 << 20, dtype=np.uint64)).astype(np.float64)
     assert abs(float(x.mean())) < 5e-3 and abs(float(x.std()) - 1.0) < 5e-3
-    assert np.abs(x).max() <= np.float32(3.4641)
+    assert np.abs(x).max() <= 6.0
+    # Irwin-Hall(12) tails, from its CDF: P(|z| > 3) = 2.014e-3 (N(0,1): 2.70e-3), P(|z| > 4) = 1.71e-5,
+    # so a 2**20 sample expects 2112 and 17.9 such values (Poisson bounds at about 4 standard deviations)
+    assert 1930 < int((np.abs(x) > 3).sum()) < 2300
+    assert 4 <= int((np.abs(x) > 4).sum()) <= 40
+    # excess kurtosis of the sum of 12 uniforms is -1.2 / 12 = -0.1
+    k = float(((x - x.mean()) ** 4).mean() / x.var() ** 2 - 3.0)
+    assert abs(k + 0.1) < 0.03
     a = synth.values16(5, 11, np.arange(1000, dtype=np.uint64), synth.BF16)
     b = synth.values16(5, 11, np.arange(1000, dtype=np.uint64), synth.BF16)
     assert np.array_equal(a, b)
