@@ -293,10 +293,10 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
                 const uint32_t addr = kb + krow * 128 + ((chunk ^ (krow & 7)) << 4);
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(addr, r0, r1, r2, r3);
-                const uint32_t a0 = e4m3x2_to<__half>((uint16_t)r0), a2 = e4m3x2_to<__half>((uint16_t)(r0 >> 16));
-                const uint32_t a1 = e4m3x2_to<__half>((uint16_t)r1), a3 = e4m3x2_to<__half>((uint16_t)(r1 >> 16));
-                const uint32_t c0 = e4m3x2_to<__half>((uint16_t)r2), c2 = e4m3x2_to<__half>((uint16_t)(r2 >> 16));
-                const uint32_t c1 = e4m3x2_to<__half>((uint16_t)r3), c3 = e4m3x2_to<__half>((uint16_t)(r3 >> 16));
+                const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)r0), a2 = e4m3x2_to_f16x2((uint16_t)(r0 >> 16));
+                const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)r1), a3 = e4m3x2_to_f16x2((uint16_t)(r1 >> 16));
+                const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)r2), c2 = e4m3x2_to_f16x2((uint16_t)(r2 >> 16));
+                const uint32_t c1 = e4m3x2_to_f16x2((uint16_t)r3), c3 = e4m3x2_to_f16x2((uint16_t)(r3 >> 16));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     mma_16816<M>(sacc[nt], a0, a1, a2, a3, qf[nt][2 * kp][0], qf[nt][2 * kp][1]);
@@ -330,8 +330,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float mnew = fmaxf(m[nt][j], mx);
                 const float muse = mnew == -INFINITY ? 0.f : mnew;
-                const float alpha = exp2f(m[nt][j] - muse);
-                const float p0 = exp2f(s0 - muse), p1 = exp2f(s1 - muse);
+                const float alpha = ex2_approx(m[nt][j] - muse);
+                const float p0 = ex2_approx(s0 - muse), p1 = ex2_approx(s1 - muse);
                 l[nt][j] = l[nt][j] * alpha + p0 + p1;
                 m[nt][j] = mnew;
                 if constexpr (KV8) {
@@ -401,10 +401,10 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t lo = rr[2 * h], hi = rr[2 * h + 1];   // keys 0-7 / 8-15 of chunk 2mp + h
-                    const uint32_t a0 = e4m3x2_to<__half>((uint16_t)__byte_perm(lo, 0u, 0x4420));
-                    const uint32_t a1 = e4m3x2_to<__half>((uint16_t)__byte_perm(lo, 0u, 0x4431));
-                    const uint32_t a2 = e4m3x2_to<__half>((uint16_t)__byte_perm(hi, 0u, 0x4420));
-                    const uint32_t a3 = e4m3x2_to<__half>((uint16_t)__byte_perm(hi, 0u, 0x4431));
+                    const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x4420));
+                    const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x4431));
+                    const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x4420));
+                    const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x4431));
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816<M>(o[2 * mp + h][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
@@ -661,8 +661,12 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(const DecodeParams
 
 // The same merge with one warp per output row, for at most 32 partitions: lane pp holds partition
 // pp's (max, sum), the weights and their sum come from warp shuffles, and each lane accumulates
-// D / 32 dims over the partitions in order. No block barrier; two dependent rounds of loads.
+// D / 32 dims over the partitions in order. No block barrier. The context length, every launched
+// partition's (max, sum) and the O of the first MERGE_SPEC partitions are loaded in one round,
+// before it is known which of them hold data: values of partitions past the context or of zero
+// weight (possibly never written) are selected away, never multiplied.
 constexpr int MERGE_ROW_WARPS = 8;
+constexpr int MERGE_SPEC = 8;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const DecodeParams p) {
@@ -673,11 +677,29 @@ __global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const 
     const int64_t row = (int64_t)blockIdx.x * MERGE_ROW_WARPS + warp;   // (b * q_len + qi) * Hq + h
     if (row >= (int64_t)p.num_seqs * p.q_len * p.Hq) return;
     const int b = (int)(row / p.Hq) / p.q_len;
+    const float *po = p.part_o + row * p.max_parts * D + lane * DL;
     int L = __ldg(p.context_lens + b);
+    const float2 v0 = lane < p.max_parts ? __ldcg(p.part_ml + row * p.max_parts + lane) : make_float2(0.f, 0.f);
+    float x[MERGE_SPEC][DL];
+#pragma unroll
+    for (int pp = 0; pp < MERGE_SPEC; ++pp) {
+        if (pp < p.max_parts) {
+            if constexpr (DL == 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)pp * D));
+                x[pp][0] = t.x, x[pp][1] = t.y, x[pp][2] = t.z, x[pp][3] = t.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < DL; ++i) x[pp][i] = __ldcg(po + (int64_t)pp * D + i);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < DL; ++i) x[pp][i] = 0.f;
+        }
+    }
     L = L < 0 ? 0 : (L > p.max_ctx ? p.max_ctx : L);
     const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
     if (nparts <= 1) return;
-    const float2 v = lane < nparts ? __ldcg(p.part_ml + row * p.max_parts + lane) : make_float2(0.f, 0.f);
+    const float2 v = lane < nparts ? v0 : make_float2(0.f, 0.f);
     float M = v.y > 0.f ? v.x : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -685,20 +707,27 @@ __global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const 
     float ds = w * v.y;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
-    const float *po = p.part_o + row * p.max_parts * D + lane * DL;
     float acc[DL];
 #pragma unroll
     for (int i = 0; i < DL; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < MERGE_SPEC; ++pp) {
+        const float c = __shfl_sync(0xffffffffu, w, pp);   // 0 for partitions past the context
+        if (c != 0.f) {
+#pragma unroll
+            for (int i = 0; i < DL; ++i) acc[i] += c * x[pp][i];
+        }
+    }
 #pragma unroll 4
-    for (int pp = 0; pp < nparts; ++pp) {
+    for (int pp = MERGE_SPEC; pp < nparts; ++pp) {
         const float c = __shfl_sync(0xffffffffu, w, pp);
         if (c == 0.f) continue;                    // an empty partition: its O is not read (it may be unwritten)
         if constexpr (DL == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)pp * D));
-            acc[0] += c * x.x;
-            acc[1] += c * x.y;
-            acc[2] += c * x.z;
-            acc[3] += c * x.w;
+            const float4 t = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)pp * D));
+            acc[0] += c * t.x;
+            acc[1] += c * t.y;
+            acc[2] += c * t.z;
+            acc[3] += c * t.w;
         } else {
 #pragma unroll
             for (int i = 0; i < DL; ++i) acc[i] += c * __ldcg(po + (int64_t)pp * D + i);
