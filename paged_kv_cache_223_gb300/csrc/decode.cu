@@ -358,16 +358,17 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             if constexpr (SPLIT_P) {
-                float hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    hi[e] = __bfloat162float(__float2bfloat16_rn(sacc[nt][e]));
-                    lo[e] = sacc[nt][e] - hi[e];
-                }
-                pb[nt][0] = movmatrix_trans(pack2<M>(hi[0], hi[1]));
-                pb[nt][1] = movmatrix_trans(pack2<M>(hi[2], hi[3]));
-                pl[nt][0] = movmatrix_trans(pack2<M>(lo[0], lo[1]));
-                pl[nt][1] = movmatrix_trans(pack2<M>(lo[2], lo[3]));
+                // a bf16 is the top half of an fp32: the high parts are unpacked from their packed pair
+                const uint32_t h01 = pack2<M>(sacc[nt][0], sacc[nt][1]);
+                const uint32_t h23 = pack2<M>(sacc[nt][2], sacc[nt][3]);
+                const uint32_t l01 = pack2<M>(sacc[nt][0] - __uint_as_float(h01 << 16),
+                                              sacc[nt][1] - __uint_as_float(h01 & 0xFFFF0000u));
+                const uint32_t l23 = pack2<M>(sacc[nt][2] - __uint_as_float(h23 << 16),
+                                              sacc[nt][3] - __uint_as_float(h23 & 0xFFFF0000u));
+                pb[nt][0] = movmatrix_trans(h01);
+                pb[nt][1] = movmatrix_trans(h23);
+                pl[nt][0] = movmatrix_trans(l01);
+                pl[nt][1] = movmatrix_trans(l23);
             } else {
                 pb[nt][0] = movmatrix_trans(pack2<M>(sacc[nt][0], sacc[nt][1]));
                 pb[nt][1] = movmatrix_trans(pack2<M>(sacc[nt][2], sacc[nt][3]));

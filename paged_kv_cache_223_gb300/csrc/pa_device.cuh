@@ -159,20 +159,23 @@ __device__ __forceinline__ void mma_16816<__nv_bfloat16>(float (&d)[4], uint32_t
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two floats -> one register of two 16-bit values (lo = first), round to nearest even.
+// Two floats -> one register of two 16-bit values (lo = first), round to nearest even: one
+// cvt.rn.{f16,bf16}x2.f32 (its first source goes to the upper half).
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 
 template <>
 __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 template <>
 __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // Two E4M3 codes (first in the low byte) -> two fp16 values (first in the low half), exactly: one
