@@ -68,6 +68,8 @@ static size_t smem_bytes(int D, int nt, bool kv8, int table_entries) {
 
 size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt, false, 0); }
 
+constexpr float DEC_RESCALE_LOG2 = 8.f;   // stale-maximum headroom of the decode softmax (P <= 2^8)
+
 template <typename T, int D, int NT, bool KV8>
 __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -316,8 +318,12 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
             }
         }
 
-        // online softmax per query column (log2 domain)
+        // online softmax per query column (log2 domain). Each column keeps a reference maximum that
+        // moves only when the tile's maximum passes it by more than 2^DEC_RESCALE_LOG2, so P <= 2^8 and
+        // O is rescaled on few tiles (O and l are relative to the reference, exactly as to a true max).
         const int t_lo = tile_t0 + gq, t_hi = t_lo + 8;
+        float alpha[NT][2];
+        bool rescale = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -328,12 +334,15 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mnew = fmaxf(m[nt][j], mx);
-                const float muse = mnew == -INFINITY ? 0.f : mnew;
-                const float alpha = ex2_approx(m[nt][j] - muse);
+                alpha[nt][j] = 1.f;
+                if (mx > m[nt][j] + DEC_RESCALE_LOG2) {   // also the first finite maximum (m = -inf)
+                    alpha[nt][j] = ex2_approx(m[nt][j] - mx);
+                    m[nt][j] = mx;
+                    rescale = true;
+                }
+                const float muse = m[nt][j] == -INFINITY ? 0.f : m[nt][j];
                 const float p0 = ex2_approx(s0 - muse), p1 = ex2_approx(s1 - muse);
-                l[nt][j] = l[nt][j] * alpha + p0 + p1;
-                m[nt][j] = mnew;
+                l[nt][j] = l[nt][j] * alpha[nt][j] + p0 + p1;
                 if constexpr (KV8) {
                     // V scale of each key row; rows past the context have no scale (select, not multiply)
                     sacc[nt][j] = t_lo < L ? p0 * vs_lo : 0.f;
@@ -342,12 +351,18 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
                     sacc[nt][j] = p0;
                     sacc[nt][2 + j] = p1;
                 }
-#pragma unroll
-                for (int md = 0; md < MT; ++md) {
-                    o[md][nt][j] *= alpha;
-                    o[md][nt][2 + j] *= alpha;
-                }
             }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int md = 0; md < MT; ++md) {
+                        o[md][nt][j] *= alpha[nt][j];
+                        o[md][nt][2 + j] *= alpha[nt][j];
+                    }
+        }
 
         // P^T as the B operand (16 keys x 8 columns): transpose the two 8x8 halves of S^T.
         // The MMA takes P in V's 16-bit type. bf16 keeps 8 mantissa bits, too few for short
