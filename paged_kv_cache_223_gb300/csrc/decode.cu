@@ -12,7 +12,8 @@
 // partition p). All q_len * G query rows that read KV head g (GQA groups;
 // q_len > 1 for verifying draft tokens) are handled together, so every K/V byte
 // of the partition is read from HBM once. The partition's tokens are cut into
-// 16-token tiles, dealt round-robin to the CTA's 4 warps. Each warp runs its own
+// 16-token tiles, dealt round-robin to the CTA's W warps (4; 2 for the short
+// suffix partitions of the shared-prefix decode). Each warp runs its own
 // STAGES-deep pipeline: its lane 0 issues TMA tile loads (128-byte swizzle, so
 // the ldmatrix reads below are bank-conflict free) completing on a per-stage
 // mbarrier, and the warp consumes tiles in order.
@@ -41,28 +42,28 @@ namespace pa {
 #define PA_FP8_STAGES 3
 #endif
 __host__ __device__ constexpr int stages_for(bool kv8) { return kv8 ? PA_FP8_STAGES : 3; }
-__host__ __device__ constexpr int min_ctas_for(bool kv8, int nt) { return kv8 && nt == 1 ? 4 : 2; }
+// CTAs per SM the launch bounds ask for: the same warps per SM whatever the warps per CTA (w)
+__host__ __device__ constexpr int min_ctas_for(bool kv8, int nt, int w) { return (kv8 && nt == 1 ? 4 : 2) * (4 / w); }
 
-// Shared memory of the tile pipelines. 16-bit pools: each stage holds the K tile then the V tile
-// (16 rows x D 16-bit values each). FP8 pools (D = 128): each stage holds the K codes tile and the V
-// codes tile (16 rows x 128 bytes each, 1024-byte aligned for the 128-byte swizzle); the stages'
-// K and V scales (16 floats each) sit in a small region after all code tiles. The codes are
-// converted to fp16 in registers, on their way from ldmatrix to the MMAs.
+// Shared memory of the tile pipelines (w warps per CTA, one pipeline each). 16-bit pools: each stage
+// holds the K tile then the V tile (16 rows x D 16-bit values each). FP8 pools (D = 128): each stage
+// holds the K codes tile and the V codes tile (16 rows x 128 bytes each, 1024-byte aligned for the
+// 128-byte swizzle); the stages' K and V scales (16 floats each) sit in a small region after all code
+// tiles. The codes are converted to fp16 in registers, on their way from ldmatrix to the MMAs.
 __host__ __device__ constexpr int stage_bytes(int D, bool kv8) { return kv8 ? 2 * TILE_TOKENS * 128 : 2 * TILE_TOKENS * D * 2; }
-__host__ __device__ constexpr int scale_region(bool kv8) { return kv8 ? DECODE_WARPS * stages_for(kv8) * 2 * TILE_TOKENS * 4 : 0; }
-__host__ __device__ constexpr int ring_bytes(int D, bool kv8) {
-    return DECODE_WARPS * stages_for(kv8) * stage_bytes(D, kv8) +
-           (kv8 ? ((scale_region(kv8) + 1023) & ~1023) : 0);
+__host__ __device__ constexpr int scale_region(bool kv8, int w) { return kv8 ? w * stages_for(kv8) * 2 * TILE_TOKENS * 4 : 0; }
+__host__ __device__ constexpr int ring_bytes(int D, bool kv8, int w) {
+    return w * stages_for(kv8) * stage_bytes(D, kv8) + (kv8 ? ((scale_region(kv8, w) + 1023) & ~1023) : 0);
 }
-__host__ __device__ constexpr int merge_bytes(int D, int nt) {
-    return DECODE_WARPS * nt * 8 * (D + 4) * 4 + DECODE_WARPS * nt * 8 * 2 * 4 + nt * 8 * (DECODE_WARPS + 2) * 4;
+__host__ __device__ constexpr int merge_bytes(int D, int nt, int w) {
+    return w * nt * 8 * (D + 4) * 4 + w * nt * 8 * 2 * 4 + nt * 8 * (w + 2) * 4;
 }
-__host__ __device__ constexpr int body_bytes(int D, int nt, bool kv8) {
-    return ring_bytes(D, kv8) > merge_bytes(D, nt) ? ring_bytes(D, kv8) : merge_bytes(D, nt);
+__host__ __device__ constexpr int body_bytes(int D, int nt, bool kv8, int w) {
+    return ring_bytes(D, kv8, w) > merge_bytes(D, nt, w) ? ring_bytes(D, kv8, w) : merge_bytes(D, nt, w);
 }
 
-static size_t smem_bytes(int D, int nt, bool kv8, int table_entries) {
-    return 1024 /* alignment slack */ + (size_t)body_bytes(D, nt, kv8) + DECODE_WARPS * stages_for(kv8) * 8 +
+static size_t smem_bytes(int D, int nt, bool kv8, int table_entries, int w = DECODE_WARPS) {
+    return 1024 /* alignment slack */ + (size_t)body_bytes(D, nt, kv8, w) + w * stages_for(kv8) * 8 +
            (size_t)table_entries * 4;
 }
 
@@ -70,8 +71,8 @@ size_t decode_smem_bytes(int head_dim, int nt) { return smem_bytes(head_dim, nt,
 
 constexpr float DEC_RESCALE_LOG2 = 8.f;   // stale-maximum headroom of the decode softmax (P <= 2^8)
 
-template <typename T, int D, int NT, bool KV8>
-__global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
+template <typename T, int D, int NT, bool KV8, int W>
+__global__ void __launch_bounds__(W * 32, min_ctas_for(KV8, NT, W))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
     static_assert(!KV8 || D == 128, "FP8 pools are built for head_dim 128");
@@ -92,8 +93,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
-    const uint32_t bars_u32 = base_u32 + body_bytes(D, NT, KV8);
-    int *tbl = reinterpret_cast<int *>(smem + body_bytes(D, NT, KV8) + DECODE_WARPS * STAGES * 8);
+    const uint32_t bars_u32 = base_u32 + body_bytes(D, NT, KV8, W);
+    int *tbl = reinterpret_cast<int *>(smem + body_bytes(D, NT, KV8, W) + W * STAGES * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -180,13 +181,13 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     }
     __syncthreads();
 
-    const int my_tiles = ntiles > warp ? (ntiles - warp + DECODE_WARPS - 1) / DECODE_WARPS : 0;
+    const int my_tiles = ntiles > warp ? (ntiles - warp + W - 1) / W : 0;
     const uint32_t ring_u32 = base_u32 + warp * STAGES * STAGE_BYTES;
-    const uint32_t scales_u32 = base_u32 + DECODE_WARPS * STAGES * STAGE_BYTES;                 // FP8 only
+    const uint32_t scales_u32 = base_u32 + W * STAGES * STAGE_BYTES;                 // FP8 only
     const uint64_t policy = l2_policy_evict_first();
 
     auto issue = [&](int it) {
-        const int i = warp + it * DECODE_WARPS;          // tile index within the partition
+        const int i = warp + it * W;          // tile index within the partition
         const int s = it % STAGES;
         const int tok = i * TILE_TOKENS;                 // token offset within the partition
         const int row0 = (tbl[tok / p.bs] * p.Hkv + g) * p.bs + (tok % p.bs);
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
             ok = false;
             break;
         }
-        const int i = warp + it * DECODE_WARPS;
+        const int i = warp + it * W;
         const int tile_t0 = t_begin + i * TILE_TOKENS;   // absolute token index of the tile's first row
         const int gq_ = lane >> 2;
         uint32_t kb = ring_u32 + s * STAGE_BYTES;
@@ -470,11 +471,11 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
         return;
     }
 
-    // ---- combine the 4 warps (smem; the tile ring is free now)
+    // ---- combine the W warps (smem; the tile ring is free now)
     constexpr int RP = NT * 8;
     constexpr int OSTR = D + 4;   // padded row: the fragment stores below hit 32 distinct banks
     float *ow = reinterpret_cast<float *>(smem);
-    float *mlw = ow + DECODE_WARPS * RP * OSTR;
+    float *mlw = ow + W * RP * OSTR;
 #pragma unroll
     for (int md = 0; md < MT; ++md)
 #pragma unroll
@@ -498,18 +499,18 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
     }
     __syncthreads();
     // per row: the running max over the warps, each warp's factor 2^(m_w - M) and the row sum, once
-    float *wsc = mlw + DECODE_WARPS * RP * 2;           // [RP][DECODE_WARPS] factors, then [RP][2] (M, sum)
-    float *rml = wsc + RP * DECODE_WARPS;
+    float *wsc = mlw + W * RP * 2;           // [RP][W] factors, then [RP][2] (M, sum)
+    float *rml = wsc + RP * W;
     for (int r = threadIdx.x; r < p.rows; r += blockDim.x) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < DECODE_WARPS; ++w) M = fmaxf(M, mlw[(w * RP + r) * 2]);
+        for (int w = 0; w < W; ++w) M = fmaxf(M, mlw[(w * RP + r) * 2]);
         const float Muse = M == -INFINITY ? 0.f : M;
         float ls = 0.f;
 #pragma unroll
-        for (int w = 0; w < DECODE_WARPS; ++w) {
+        for (int w = 0; w < W; ++w) {
             const float sc = exp2f(mlw[(w * RP + r) * 2] - Muse);
-            wsc[r * DECODE_WARPS + w] = sc;
+            wsc[r * W + w] = sc;
             ls += sc * mlw[(w * RP + r) * 2 + 1];
         }
         rml[r * 2] = M;
@@ -528,8 +529,8 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, min_ctas_for(KV8, NT))
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
-        for (int w = 0; w < DECODE_WARPS; ++w) {
-            const float sc = wsc[r * DECODE_WARPS + w];
+        for (int w = 0; w < W; ++w) {
+            const float sc = wsc[r * W + w];
             const float4 a = *reinterpret_cast<const float4 *>(ow + (w * RP + r) * OSTR + d0);
             const float4 c = *reinterpret_cast<const float4 *>(ow + (w * RP + r) * OSTR + d0 + 4);
             acc[0] += sc * a.x;
@@ -761,26 +762,39 @@ __global__ void __launch_bounds__(MERGE_ROW_WARPS * 32) merge_rows_kernel(const 
 
 // ------------------------------------------------------------------ launchers
 
-template <typename T, int D, int NT, bool KV8>
+template <typename T, int D, int NT, bool KV8, int W>
 static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t stream) {
-    const size_t smem = smem_bytes(D, NT, KV8, (p.part_tokens + p.bs - 1) / p.bs);
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = smem_bytes(D, NT, KV8, (p.part_tokens + p.bs - 1) / p.bs, W);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, NT, KV8, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)p.num_seqs * p.Hkv * (p.max_parts - p.part0);
-    e = launch_pdl(decode_kernel<T, D, NT, KV8>, dim3((unsigned)grid), dim3(DECODE_WARPS * 32), smem, stream, tmk, tmv, p);
+    e = launch_pdl(decode_kernel<T, D, NT, KV8, W>, dim3((unsigned)grid), dim3(W * 32), smem, stream, tmk, tmv, p);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Warps per CTA: 4, except for the suffix pass of the shared-prefix decode, whose (sequence, KV head)
+// units hold a few hundred tokens each. There each CTA's fixed costs (query, context length and
+// block-table loads, the pipeline fill, the combine of the warps' states) weigh on few tiles per warp;
+// two-warp CTAs (twice the CTAs per SM) give each warp twice the tiles: 0.068 -> 0.065 ms on the
+// shared-prefix verify workload. One warp per CTA, or two elsewhere, measured slower or no faster.
+template <typename T, int D, int NT, bool KV8>
+static cudaError_t launch_decode_w(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t stream) {
+    if constexpr (!KV8 && D == 128)
+        if (p.part0 > 0) return launch_decode_t<T, D, NT, KV8, 2>(p, tmk, tmv, stream);
+    return launch_decode_t<T, D, NT, KV8, DECODE_WARPS>(p, tmk, tmv, stream);
 }
 
 template <typename T, int D, bool KV8>
 static cudaError_t launch_decode_d(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t stream) {
     switch ((p.rows + 7) / 8) {
-        case 1: return launch_decode_t<T, D, 1, KV8>(p, tmk, tmv, stream);
-        case 2: return launch_decode_t<T, D, 2, KV8>(p, tmk, tmv, stream);
-        case 3: return launch_decode_t<T, D, 3, KV8>(p, tmk, tmv, stream);
-        case 4: return launch_decode_t<T, D, 4, KV8>(p, tmk, tmv, stream);
+        case 1: return launch_decode_w<T, D, 1, KV8>(p, tmk, tmv, stream);
+        case 2: return launch_decode_w<T, D, 2, KV8>(p, tmk, tmv, stream);
+        case 3: return launch_decode_w<T, D, 3, KV8>(p, tmk, tmv, stream);
+        case 4: return launch_decode_w<T, D, 4, KV8>(p, tmk, tmv, stream);
         default: return cudaErrorInvalidValue;
     }
 }
