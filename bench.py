@@ -375,7 +375,9 @@ def run_gpu(args):
 
 def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier, kv_format: int = 0):
     """Same step through the Python binding with per-step inputs copied from pinned host memory and the outputs
-    read back, all inside the timed region."""
+    read back, all inside the timed region. The copies run on two copy streams, so a layer's inputs travel
+    while earlier layers compute and its output returns while later layers compute (each layer has its own
+    device buffers); every step ends with the host holding all of that step's outputs."""
     import torch
     host = []
     for L in G.layers:
@@ -383,15 +385,28 @@ def run_e2e(G: GpuWorkload, wl: synth.Workload, dev, steps: int, barrier, kv_for
         host[-1]["out"] = torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for hl in host for k, t in hl.items() if k != "out")
     d2h = sum(hl["out"].numel() * hl["out"].element_size() for hl in host)
+    main = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in G.layers]
+    ev_done = [torch.cuda.Event() for _ in G.layers]
 
     def one():
-        for L, hl in zip(G.layers, host):
-            for k in ("kn", "vn", "slots", "q", "tables", "lens"):
-                L[k].copy_(hl[k], non_blocking=True)
+        up.wait_stream(main)     # the previous step has been read back (synchronised below); nothing in flight
+        with torch.cuda.stream(up):
+            for i, (L, hl) in enumerate(zip(G.layers, host)):
+                for k in ("kn", "vn", "slots", "q", "tables", "lens"):
+                    L[k].copy_(hl[k], non_blocking=True)
+                ev_in[i].record(up)
+        for i, (L, hl) in enumerate(zip(G.layers, host)):
+            main.wait_event(ev_in[i])
             G.pool.cache_write(L["kn"], L["vn"], L["slots"], L["kc"], L["vc"])
             G.decode(L)
-            hl["out"].copy_(L["out"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+            ev_done[i].record(main)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[i])
+                hl["out"].copy_(L["out"], non_blocking=True)
+        down.synchronize()
+        main.synchronize()
 
     one()
     barrier()
