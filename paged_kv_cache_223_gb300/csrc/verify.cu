@@ -36,6 +36,11 @@
 //   warp 4      MMA issue (one thread) and tensor-memory allocation.
 //   warp 5      item fetch (one thread): the next item and its sequence's context length into a ring
 //               that every role reads.
+//   warp 6      V rows past an item: follows every V copy as it lands; in an item's last, partial tile it
+//               zeroes the rows past the item (they may hold other data, NaN included, and a zero weight
+//               times NaN is NaN); then it releases the tile's P.V. Done by the softmax before, it made the
+//               softmax of every item's last tile wait for that tile's V copy, which lands about a tile after
+//               K: ~4,000 cycles on the MMA chain per item.
 //   warps 8-11  K producers, warps 12-15 V producers: each warp copies two 16-key sub-tiles of every
 //               tile, one TMA box per 64-dimension half; block ids looked up one tile ahead (one warp's
 //               copies are issued one after another, and TMA throughput scales with issuing warps).
@@ -64,20 +69,22 @@ constexpr int VF_LOOKAHEAD = 2;                        // items a CTA holds ahea
 constexpr int VF_OFF_RING = VF_OFF_X + 3 * VF_ROWS * 4 * 4;   // item ring: (item index or -1, context length)
 constexpr int VF_OFF_BAR = VF_OFF_RING + VF_QSLOTS * 8;
 // barriers: k_full[2] k_empty[2] v_full[2] v_empty[2] q_full[2] q_free[2] s_full[2] p_full[2] pv_done[2]
-//           o_full o_free mx lx ost drain item_full[8] item_empty[8]
-constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6 + 2 * VF_QSLOTS;
-// roles that read every item of the ring: 4 K producer warps, 4 V producer warps, the MMA thread, 4 softmax warps
-constexpr int VF_ITEM_READERS = 13;
+//           o_full o_free mx lx ost drain v_fixed[2] item_full[8] item_empty[8]
+constexpr int VF_NBAR = 2 * VF_KSTAGES + 2 * VF_VSTAGES + 5 * 2 + 6 + 2 + 2 * VF_QSLOTS;
+// roles that read every item of the ring: 4 K producer warps, 4 V producer warps, the MMA thread, 4 softmax warps,
+// the V-row warp
+constexpr int VF_ITEM_READERS = 14;
 constexpr int VF_OFF_MISC = VF_OFF_BAR + VF_NBAR * 8;  // tmem slot, abort flag, issued counters [2][4], items taken
 constexpr int VF_SMEM = 1024 + VF_OFF_MISC + 64;
 static_assert(VF_OFF_BAR % 8 == 0, "barrier alignment");
 static_assert(VF_SMEM <= 227 * 1024, "verify shared memory");
 
-// 16 warps; warp 5 fetches the CTA's items, warps 6-7 only take part in the prologue and teardown. Launched at 128 registers per thread;
+// 16 warps; warp 5 fetches the CTA's items, warp 6 zeroes V rows past the items, warp 7 only takes part in the
+// prologue and teardown. Launched at 128 registers per thread;
 // the softmax warpgroup raises its share and the other three lower theirs (setmaxnreg):
 // 128 x 232 + 384 x 88 <= 512 x 128.
 constexpr int VF_THREADS = 512;
-constexpr int VF_MMA_WARP = 4, VF_SCHED_WARP = 5, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
+constexpr int VF_MMA_WARP = 4, VF_SCHED_WARP = 5, VF_VFIX_WARP = 6, VF_KPROD_WARP = 8, VF_VPROD_WARP = 12;
 constexpr uint32_t VF_REGS_HIGH = 232, VF_REGS_LOW = 88;
 static_assert(128 * VF_REGS_HIGH + 384 * VF_REGS_LOW <= VF_THREADS * 128, "register split");
 // tensor memory: Q4[2] at columns 0 / 64 (128 d as 64 packed columns), S[2] at 128 / 256, O^T at 384 (64 columns)
@@ -234,7 +241,8 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
     const uint32_t bar_lx = bar_mx + 8;
     const uint32_t bar_ost = bar_lx + 8;
     const uint32_t bar_drain = bar_ost + 8;
-    const uint32_t bar_item_full = bar_drain + 8;
+    const uint32_t bar_v_fixed = bar_drain + 8;   // [2 stages]: the V tile is ready for its P.V (rows past the item zeroed)
+    const uint32_t bar_item_full = bar_v_fixed + 16;
     const uint32_t bar_item_empty = bar_item_full + VF_QSLOTS * 8;
     int2 *item_ring = reinterpret_cast<int2 *>(smem + VF_OFF_RING);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + VF_OFF_MISC);
@@ -276,6 +284,8 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
         mbar_init(bar_lx, 128);
         mbar_init(bar_ost, 128);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_v_fixed, 32);
+        mbar_init(bar_v_fixed + 8, 32);
         for (int s = 0; s < VF_QSLOTS; ++s) {
             mbar_init(bar_item_full + s * 8, 1);
             mbar_init(bar_item_empty + s * 8, VF_ITEM_READERS);
@@ -414,6 +424,10 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                                  abort_flag))
                         return false;
                     consumed_v = pv_jj + 1;
+                    // the V-row warp has seen the tile land (and zeroed the rows past the item of a partial tile)
+                    if (!vf_wait(bar_v_fixed + (pv_jj % VF_VSTAGES) * 8, (uint32_t)(pv_jj / VF_VSTAGES) & 1u, p.wait_ns,
+                                 abort_flag))
+                        return false;
                     // the item's first product overwrites O: the previous item's epilogue must have read it
                     if (pv_first && pv_ii >= 1 &&
                         !vf_wait(bar_o_free, (uint32_t)(pv_ii - 1) & 1u, p.wait_ns, abort_flag))
@@ -502,6 +516,40 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                     if (idx < 0) break;
                 }
             }
+            __syncwarp();
+        } else if (warp == VF_VFIX_WARP) {
+            // ------------------------------------------------------------------ V rows past an item
+            // Every V tile, in order: wait for its copy, zero the rows past the item in a partial tile, release its
+            // P.V (v_fixed has the stages and phases of v_full). Waiting on every tile keeps this warp from running
+            // ahead of the copies (a parity wait two phases ahead would pass at once), and since the P.V of each
+            // tile waits for this release, no copy into the stage can land before this warp has seen the one before.
+            int jj = 0;
+            bool ok = true;
+            VfItems items(p, item_ring, bar_item_full, bar_item_empty, abort_flag, nlaunch, true);
+            VfItem it;
+            while (ok) {
+                const int got = items.next(it);
+                if (got <= 0) {
+                    ok = got == 0;
+                    break;
+                }
+                for (int t = 0; t < it.ntiles; ++t, ++jj) {
+                    ok = __all_sync(0xffffffffu, vf_wait(bar_v_full + (jj % VF_VSTAGES) * 8,
+                                                         (uint32_t)(jj / VF_VSTAGES) & 1u, p.wait_ns, abort_flag, 64));
+                    if (!ok) break;
+                    const int nvalid = it.t_end - (it.t_begin + t * VF_KT);
+                    if (nvalid < VF_KT) {
+                        uint8_t *vt = smem + VF_OFF_V + (jj % VF_VSTAGES) * VF_TILE_BYTES;
+                        // two rows per step: a row is 2 x 128 bytes (both 64-dimension halves), 16 lanes x 16 bytes
+                        for (int c = nvalid + (lane >> 4); c < VF_KT; c += 2)
+                            *reinterpret_cast<uint4 *>(vt + ((lane >> 3) & 1) * VF_HALF_BYTES + c * 128 +
+                                                       (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();   // the zeroed rows are read by the tensor cores
+                    }
+                    mbar_arrive(bar_v_fixed + (jj % VF_VSTAGES) * 8);
+                }
+            }
+            if (!ok) *abort_flag = 1;
             __syncwarp();
         }
     } else {
@@ -626,22 +674,7 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                                          : "memory");
                     }
                 }
-                if (nvalid < VF_KT && warp == 0) {
-                    // keys past the item: their V rows hold other data (possibly NaN): zero them once the tile has
-                    // landed, so that a zero weight times the row stays zero
-                    ok = __all_sync(0xffffffffu, vf_wait(bar_v_full + (jj % VF_VSTAGES) * 8,
-                                                         (uint32_t)(jj / VF_VSTAGES) & 1u, p.wait_ns, abort_flag));
-                    if (!ok) break;
-                    uint8_t *vt = smem + VF_OFF_V + (jj % VF_VSTAGES) * VF_TILE_BYTES;
-                    for (int c = nvalid + lane; c < VF_KT; c += 32) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            *reinterpret_cast<uint4 *>(vt + c * 128 + k * 16) = make_uint4(0u, 0u, 0u, 0u);
-                            *reinterpret_cast<uint4 *>(vt + VF_HALF_BYTES + c * 128 + k * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();   // the weights (and zeroed V rows) are read by the tensor cores
+                fence_proxy_async_smem();   // the weights are read by the tensor cores
                 tc_fence_before();
                 mbar_arrive(bar_p_full + (jj & 1) * 8);
             }
