@@ -588,7 +588,6 @@ __global__ void __launch_bounds__(VF_THREADS, 1)
                 tmem_ld_cols<VF_SW>(scol + slice * VF_SW, sv);
                 const int t0 = it.t_begin + t * VF_KT;
                 const int k0 = t0 + slice * VF_SW;            // absolute index of the slice's first key
-                const int nvalid = it.t_end - t0;             // keys of this tile inside the item (>= 1)
                 // last visible key of this row in the slice (keys past the item or the row's limit are masked)
                 const int cut = min(it.t_end - 1, lim) - k0;
                 float m4[4];
