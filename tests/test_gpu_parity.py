@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 import synth.device as sdev
 from paged_kv_cache_223_gb300 import pagedattn as pa
@@ -124,3 +125,44 @@ def test_stress_variants(stress):
         out = pool.decode(q, tables, lens, wl.scale, k_cache=kc, v_cache=vc)
         ref, _, _ = H.oracle_reference(wl, 0)
         H.assert_close(out, ref, f"cfg{k} {stress}")
+
+
+def _scaled_words(words: np.ndarray, factor: np.ndarray, dtype: int) -> np.ndarray:
+    """16-bit words times a float32 factor, rounded to nearest even (test-side: builds inputs, not expected values)."""
+    if dtype == synth.FP16:
+        return (words.view(np.float16).astype(np.float32) * factor).astype(np.float16).view(np.uint16)
+    f = (words.astype(np.uint32) << 16).view(np.float32) * factor
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+# (lens, Hq, Hkv, q_len, dtype): one 8-column tile of rows on the mma.sync decode, and 20 rows on the
+# tensor-core decode; contexts over several partitions
+RISING = [([1500, 3000, 700], 64, 8, 1, synth.FP16), ([900, 2100, 1300], 32, 8, 5, synth.BF16)]
+
+
+@pytest.mark.parametrize("case", RISING, ids=["decode_g8", "verify_20rows"])
+def test_rising_scores_move_the_softmax_reference(case):
+    """Keys scaled by 1 + 15 t / L along each context, so that the scores' spread grows from N(0,1) to 16
+    sigma: every row's running maximum passes its reference by more than 2^8 several times, in late tiles and
+    partitions too, which makes the kernels rescale O and the merge combine partitions whose references differ
+    widely."""
+    lens, Hq, Hkv, q_len, dt = case
+    wl = synth.custom_workload(lens, Hq, Hkv, 128, 16, q_len, dt, tag=360 + RISING.index(case))
+    pool, kc, vc, q, tables, lens_d = H.build_device(wl)
+    _, hk, hv = H.oracle_reference(wl, 0)
+    kw = kc.view(torch.int16)
+    for b, L in enumerate(wl.context_lens):
+        t = np.arange(int(L))
+        slots = wl.slots(b, t)
+        blk, off = slots // wl.bs, slots % wl.bs
+        factor = (1.0 + 15.0 * t / float(L)).astype(np.float32)[:, None, None]
+        words = _scaled_words(hk[blk, :, off, :], factor, dt)
+        hk[blk, :, off, :] = words
+        kw[torch.from_numpy(blk).to(H.DEV), :, torch.from_numpy(off).to(H.DEV), :] = \
+            torch.from_numpy(words.view(np.int16)).to(H.DEV)
+    out = pool.decode(q, tables, lens_d, wl.scale, k_cache=kc, v_cache=vc)
+    assert pool.check() == pa.PA_OK
+    ref, _ = oracle.paged_attention(wl.q_values(0), hk, hv, wl.block_tables, wl.context_lens, wl.dtype, wl.scale)
+    H.assert_close(out, ref, f"rising scores {case}")
+
