@@ -35,17 +35,15 @@
 
 namespace pa {
 
-// Pipeline depth per warp and resident CTAs per SM: 16-bit stages are 8 KB (3 stages, 2 CTAs per
-// SM); FP8 stages are 4 KB (3 stages), with 4 single-column-tile CTAs per SM (16 warps) to hide the
-// latency of each tile's code conversions.
-#ifndef PA_FP8_STAGES
-#define PA_FP8_STAGES 3
-#endif
 // Pipeline stages per warp and CTAs per SM (the launch bounds; the same warps per SM whatever the warps
-// per CTA, w). 16-bit pools with one 8-column tile of query rows: 2 stages and 3 CTAs per SM (12 warps,
-// 64 KB of tiles per CTA). 3 stages at 2 CTAs per SM keep more bytes in flight per warp but fewer warps
-// and CTAs to cover each CTA's start and end. Same box, six rounds against that shape: Llama-3-8B-shaped
-// 0-4% faster, 70B-shaped layer and long context 0-2% faster, none slower.
+// per CTA, w). 16-bit stages hold 8 KB of K+V at head_dim 128, FP8 stages 4 KB of codes.
+// - 16-bit pools with one 8-column tile of query rows: 2 stages and 3 CTAs per SM (12 warps, 64 KB of
+//   tiles per CTA). 3 stages at 2 CTAs per SM keep more bytes in flight per warp but fewer warps and
+//   CTAs to cover each CTA's start and end. Same box, six rounds against that shape: Llama-3-8B-shaped
+//   0-4% faster, 70B-shaped layer and long context 0-2% faster, none slower.
+// - More 16-bit rows: 3 stages at 2 CTAs per SM (the registers of 16-32 rows allow no more).
+// - FP8 pools: 3 stages, 4 single-column-tile CTAs per SM (16 warps).
+constexpr int PA_FP8_STAGES = 3;
 __host__ __device__ constexpr int stages_for(bool kv8, int nt) { return kv8 ? PA_FP8_STAGES : (nt == 1 ? 2 : 3); }
 __host__ __device__ constexpr int min_ctas_for(bool kv8, int nt, int w) {
     return (kv8 && nt == 1 ? 4 : (!kv8 && nt == 1 ? 3 : 2)) * (4 / w);
