@@ -105,12 +105,18 @@ __global__ void __launch_bounds__(W * 32, min_ctas_for(KV8, NT, W))
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nlaunch = p.max_parts - p.part0;         // partitions launched per (sequence, KV head)
-    const int part = p.part0 + (int)(blockIdx.x % nlaunch);
+    // CTA order over (unit = (sequence, KV head), partition): 16-bit pools take a unit's partitions one
+    // after another; FP8 pools take every unit's last partition first, then the one before, and so on.
+    // Measured on one box, three rounds: for FP8 the Llama-3-8B-shaped and long-context decodes were ~2%
+    // faster that way and the 70B-shaped one unchanged; for 16-bit pools it was no faster (0-1% slower),
+    // and partition-major in ascending order was 2-4% slower.
+    const int units = (int)(gridDim.x / nlaunch);
+    const int part = KV8 ? p.part0 + (nlaunch - 1 - (int)(blockIdx.x / units)) : p.part0 + (int)(blockIdx.x % nlaunch);
+    const int bg = KV8 ? (int)(blockIdx.x % units) : (int)(blockIdx.x / nlaunch);
     // launched with programmatic serialization: the merge behind this kernel may be launched now (its CTAs
     // take only what this grid leaves free and wait for its end); this kernel waits for the work ahead of it
     pdl_trigger();
     pdl_wait();
-    const int bg = blockIdx.x / nlaunch;
     const int g = bg % p.Hkv;
     const int b = bg / p.Hkv;
 
